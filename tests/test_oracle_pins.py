@@ -1,0 +1,390 @@
+"""Pins for the CPU oracle: each check ties it to something other than
+itself -- hand-derived values, brute force, closed forms, invariants and
+library routines (numpy's binary16 conversion, torch's fp64 matmul, exact
+rational arithmetic).
+
+Method: Dong et al., "Efficient LLM ad generation via model compression and
+parallel verification" (arXiv 2605.11582), section 3.2 (sparsification,
+Eq. 3; adaptive group quantization) and section 1 (contribution 1, the
+2bit-CSR format).
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import synth
+
+
+# ---------------------------------------------------------------------------
+# binary16 conversions against numpy's implementation of IEEE-754 binary16.
+# ---------------------------------------------------------------------------
+
+def test_f16_to_f64_exhaustive(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.f16_bits_to_f64(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # the sign of zero survives
+    assert math.copysign(1.0, orc.f16_bits_to_f64(0x8000)) == -1.0
+
+
+def _ties_and_neighbours():
+    """Every midpoint between adjacent finite binary16 values (positive and
+    negative), plus each midpoint nudged by one binary64 ulp either way."""
+    pos = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16)
+    v = pos.view(np.float16).astype(np.float64)
+    mids = (v[:-1] + v[1:]) / 2.0           # exact in binary64
+    top = np.array([65504.0 + 16.0])        # midpoint to the overflow threshold
+    mids = np.concatenate([mids, top])
+    up = np.nextafter(mids, np.inf)
+    dn = np.nextafter(mids, -np.inf)
+    allv = np.concatenate([mids, up, dn])
+    return np.concatenate([allv, -allv])
+
+
+def test_f64_to_f16_ties_to_even(orc):
+    vals = _ties_and_neighbours()
+    sample = vals[:: max(1, vals.size // 20000)]
+    with np.errstate(over="ignore"):
+        ref = sample.astype(np.float16).view(np.uint16)
+    got = np.array([orc.f64_to_f16_bits(float(v)) for v in sample],
+                   dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_f64_to_f16_specials(orc):
+    cases = [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6,
+             2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -26, 1e-30,
+             5e-324, float("inf"), float("-inf"), 2.0 ** -14,
+             2.0 ** -14 - 2.0 ** -25]
+    with np.errstate(over="ignore"):
+        ref = np.array(cases, dtype=np.float64).astype(np.float16).view(np.uint16)
+    got = np.array([orc.f64_to_f16_bits(v) for v in cases], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    assert orc.f64_to_f16_bits(float("nan")) & 0x7C00 == 0x7C00
+    assert orc.f64_to_f16_bits(float("nan")) & 0x3FF != 0
+
+
+def test_f32_to_f16_random(orc):
+    g = synth.rng(7)
+    x = (g.standard_normal(20000) * np.exp2(g.integers(-28, 18, 20000))).astype(np.float32)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = np.array([orc.f32_to_f16_bits(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------------------
+# O1 pruning: brute force and the Eq. 3 special case.
+# ---------------------------------------------------------------------------
+
+def _brute_keep(quad, n):
+    """The unique N-subset S with: every kept element beats every dropped
+    one (strictly larger |w|, or equal |w| and lower column)."""
+    a = [abs(float(v)) for v in quad]
+    found = []
+    for S in itertools.combinations(range(4), n):
+        ok = all(a[i] > a[j] or (a[i] == a[j] and i < j)
+                 for i in S for j in range(4) if j not in S)
+        if ok:
+            found.append(S)
+    assert len(found) == 1
+    return found[0]
+
+
+@pytest.mark.parametrize("n_keep", [1, 2])
+def test_prune_exhaustive_small_alphabet(orc, n_keep):
+    # every quad over an alphabet with ties, signed zeros and sign flips
+    alphabet = [0.0, -0.0, 0.5, -0.5, 1.0, -1.0, 2.0]
+    quads = np.array(list(itertools.product(alphabet, repeat=4)),
+                     dtype=np.float32)                     # 2401 x 4
+    W = quads.reshape(1, -1)
+    pos = orc.prune(W, n_keep).reshape(-1, n_keep)
+    for t, quad in enumerate(quads):
+        assert tuple(pos[t]) == _brute_keep(quad, n_keep)
+
+
+@pytest.mark.parametrize("n_keep", [1, 2])
+def test_prune_invariants_random(orc, n_keep):
+    W = synth.weight_outliers(3, 17, 64)
+    pos = orc.prune(W, n_keep)
+    assert pos.shape == (17, 16, n_keep)
+    assert (pos < 4).all()
+    if n_keep == 2:
+        assert (pos[..., 0] < pos[..., 1]).all()
+    # kept magnitudes dominate dropped magnitudes in every quad
+    for r in range(17):
+        for t in range(16):
+            q = np.abs(W[r, 4 * t:4 * t + 4])
+            kept = set(pos[r, t].tolist())
+            drop = [i for i in range(4) if i not in kept]
+            assert min(q[list(kept)]) >= max(q[drop])
+
+
+def test_prune_is_eq3_with_constant_norm_and_no_gradient(orc):
+    """Eq. 3 scores |W_ij| * ||X_j||_2 + |W_ij| * |dE/dW_ij|.  With every
+    input-channel norm equal and the gradient term zero, keeping the top-N
+    scores per quad is exactly the oracle's magnitude pruning."""
+    W = synth.weight_normal(5, 8, 128, 0.02)
+    xnorm = np.full(128, 3.7)
+    grad = np.zeros_like(W)
+    score = np.abs(W) * xnorm + np.abs(W) * np.abs(grad)
+    for n_keep in (1, 2):
+        pos = orc.prune(W, n_keep)
+        for r in range(8):
+            for t in range(32):
+                s = score[r, 4 * t:4 * t + 4]
+                want = sorted(np.argsort(-s, kind="stable")[:n_keep].tolist())
+                assert pos[r, t].tolist() == want
+
+
+def test_prune_rejects_nonfinite(orc):
+    for bad in (np.nan, np.inf, -np.inf):
+        W = np.zeros((2, 8), np.float32)
+        W[1, 5] = bad
+        with pytest.raises(orc.OracleError) as e:
+            orc.prune(W, 2)
+        assert e.value.code == orc.ORC_ERR_NONFINITE
+
+
+# ---------------------------------------------------------------------------
+# Hand-derived tiny cases: prune + quantise + encode + dequant + matvec.
+# ---------------------------------------------------------------------------
+
+def test_hand_case_2of4(orc):
+    # quad0 |w| = .1 .5 .3 0 -> keep positions 1, 2 (values -0.5, 0.3)
+    # quad1 |w| = 2 2 2 1   -> three-way tie, lower columns win: 0, 1
+    W = np.array([[0.1, -0.5, 0.3, 0.0, 2.0, 2.0, -2.0, 1.0]], np.float32)
+    p = orc.pack(W, n_keep=2, group=8)
+    # group values {-0.5, 0.3, 2, 2}: lo = -0.5, hi = 2, (hi-lo)/15 =
+    # 0.16666667f -> binary16 1365 * 2^-13 = 0.1666259765625 (bits 0x3155)
+    assert p.scale.tolist() == [[0x3155]]
+    # z = rint(0.5 / 0.16662598) = rint(3.0007) = 3  (binary16 3.0 = 0x4200)
+    assert p.zero.tolist() == [[0x4200]]
+    # q = rint(w/s) + 3: -0.5 -> -3+3 = 0; 0.3 -> 2+3 = 5; 2.0 -> 12+3 = 15
+    # vals: j0|j1<<4 = 0x50, j2|j3<<4 = 0xFF; idx: 1 | 2<<2 | 0<<4 | 1<<6
+    assert p.vals.tolist() == [[0x50, 0xFF]]
+    assert p.idx.tolist() == [[0x49]]
+    s = 1365 / 8192
+    want = [0, -3 * s, 2 * s, 0, 12 * s, 12 * s, 0, 0]
+    assert orc.dequant(p).tolist() == [want]
+    y = orc.matvec(p, np.ones((1, 8), np.float16))
+    assert y.tolist() == [[3.8323974609375]]
+
+
+def test_hand_case_1of4(orc):
+    W = np.array([[0.0, -0.0, 0.0, 0.0,      # all equal: position 0 kept
+                   1.0, -3.0, 3.0, 2.0,      # |3| tie: position 1 kept
+                   0.25, 0.5, 0.75, -0.75,   # |.75| tie: position 2 kept
+                   -1.0, 0.5, 0.5, 0.5]],    # position 0 kept
+                 np.float32)
+    p = orc.pack(W, n_keep=1, group=16)
+    # S = {0, -3, .75, -1}: lo = -3, hi = .75, s = 3.75/15 = 0.25 exactly
+    assert p.scale.tolist() == [[0x3400]]
+    # z = rint(3 / .25) = 12 (binary16 0x4A00); q = [12, 0, 15, 8]
+    assert p.zero.tolist() == [[0x4A00]]
+    assert p.vals.tolist() == [[0x0C, 0x8F]]
+    assert p.idx.tolist() == [[0x24]]      # 0 | 1<<2 | 2<<4 | 0<<6
+    want = np.zeros(16)
+    want[5], want[10], want[12] = -3.0, 0.75, -1.0
+    assert orc.dequant(p).tolist() == [want.tolist()]
+
+
+# ---------------------------------------------------------------------------
+# O2 quantisation: closed forms and error bounds.
+# ---------------------------------------------------------------------------
+
+def test_quant_exact_grid_roundtrip(orc):
+    """Kept values already on the grid k * 2^-6, spanning exactly 15 steps
+    with 0 inside, come back exactly: s = 2^-6 and z = -lo / s.  Dropped
+    slots hold 0, so ties send the kept pair to positions 0 and 1."""
+    g = synth.rng(11)
+    step = 2.0 ** -6
+    for z0 in (0, 3, 7, 15):
+        ks = g.integers(-z0, 16 - z0, size=(4, 64))
+        ks[:, 0], ks[:, 1] = -z0, 15 - z0      # pin the range ends
+        W = np.zeros((4, 32, 4), np.float32)
+        W[:, :, 0] = ks[:, 0::2] * step
+        W[:, :, 1] = ks[:, 1::2] * step
+        W = W.reshape(4, 128)
+        p = orc.pack(W, n_keep=2, group=128)
+        s = np.array([orc.f16_bits_to_f64(b) for b in p.scale.ravel()])
+        z = np.array([orc.f16_bits_to_f64(b) for b in p.zero.ravel()])
+        assert (s == step).all() and (z == z0).all()
+        assert np.array_equal(orc.dequant(p), W.astype(np.float64))
+
+
+def test_quant_bounds_random(orc):
+    for n_keep, group in ((2, 64), (2, 128), (1, 256), (1, 64)):
+        W = synth.weight_outliers(21 + group, 6, 512)
+        pos = orc.prune(W, n_keep)
+        q, scale, zero = orc.quantize(W, pos, n_keep, group)
+        assert q.max() <= 15
+        P = 512 // 4 * n_keep
+        per_group = group // 4 * n_keep
+        for r in range(6):
+            for G in range(512 // group):
+                s = orc.f16_bits_to_f64(scale[r, G])
+                z = orc.f16_bits_to_f64(zero[r, G])
+                assert z == int(z) and 0 <= z <= 15
+                assert s > 0
+                js = range(G * per_group, (G + 1) * per_group)
+                for j in js:
+                    t = j // n_keep
+                    w = float(W[r, 4 * t + int(pos[r, t, j % n_keep])])
+                    wh = (int(q[r, j]) - z) * s
+                    assert abs(w - wh) <= s * (1 + 1e-6)
+                    if 0 < q[r, j] < 15:
+                        assert abs(w - wh) <= 0.5 * s * (1 + 1e-5)
+        assert q.shape == (6, P)
+
+
+def test_quant_special_groups(orc):
+    # all-zero group: s = 1.0, z = 0, q = 0
+    W = np.zeros((1, 64), np.float32)
+    p = orc.pack(W, 2, 64)
+    assert p.scale.tolist() == [[0x3C00]] and p.zero.tolist() == [[0]]
+    assert not p.vals.any()
+    # all-positive group: lo = 0 -> z = 0; all-negative: hi = 0 -> z = 15
+    Wp = np.abs(synth.weight_normal(2, 1, 64, 0.02))
+    Wn = -Wp
+    assert orc.pack(Wp, 2, 64).zero.tolist() == [[0]]
+    assert orc.f16_bits_to_f64(orc.pack(Wn, 2, 64).zero[0, 0]) == 15.0
+    # tiny values: (hi-lo)/15 underflows binary16 -> s = 2^-24
+    Wt = np.full((1, 64), 1e-12, np.float32)
+    pt = orc.pack(Wt, 2, 64)
+    assert pt.scale.tolist() == [[0x0001]]
+    # huge values: scale beyond binary16 -> range error
+    Wh = np.full((1, 64), 3e6, np.float32)
+    with pytest.raises(orc.OracleError) as e:
+        orc.pack(Wh, 2, 64)
+    assert e.value.code == orc.ORC_ERR_RANGE
+
+
+# ---------------------------------------------------------------------------
+# O3 / O4: encoding round trip and dense reconstruction.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n_keep,group", [(2, 64), (1, 128), (2, 256), (1, 64)])
+def test_encode_roundtrip_and_dense(orc, n_keep, group):
+    rows, cols = 5, 768
+    W = synth.weight_outliers(40 + group + n_keep, rows, cols)
+    pos = orc.prune(W, n_keep)
+    q, scale, zero = orc.quantize(W, pos, n_keep, group)
+    vals, idx = orc.encode(pos, q, rows, cols, n_keep)
+    vb, ib = orc.row_bytes(cols, n_keep)
+    P = cols // 4 * n_keep
+    assert vals.shape == (rows, P // 2) and idx.shape == (rows, P // 4)
+    pos2, q2 = orc.decode(vals, idx, rows, cols, n_keep)
+    assert np.array_equal(pos2, pos.reshape(rows, P))
+    assert np.array_equal(q2, q)
+    # dense matrix built here straight from (pos, q, s, z), before encoding
+    dense = np.zeros((rows, cols))
+    for r in range(rows):
+        for j in range(P):
+            t = j // n_keep
+            c = 4 * t + int(pos[r, t, j % n_keep])
+            G = c // group
+            s = orc.f16_bits_to_f64(scale[r, G])
+            z = orc.f16_bits_to_f64(zero[r, G])
+            dense[r, c] = (int(q[r, j]) - z) * s
+    p = orc.Packed(rows, cols, n_keep, group, vals, idx, scale, zero)
+    dq = orc.dequant(p)
+    assert np.array_equal(dq, dense)
+    # quad invariant: at most N nonzeros per quad, only at stored positions
+    nz = (dq.reshape(rows, cols // 4, 4) != 0)
+    assert (nz.sum(axis=2) <= n_keep).all()
+
+
+def test_csr_size_ratio_matches_paper(orc):
+    """Section 1, contribution 1: indices + weights shrink to 30% of the
+    original CSR.  With INT4 values and 16-bit column indices as the
+    original CSR, the canonical 2bit-CSR row reproduces that ratio."""
+    import os
+    here = os.path.dirname(__file__)
+    ratio = None
+    with open(os.path.join(here, "golden", "csr_size_ratio.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                ratio = float(line)
+    for n_keep in (1, 2):
+        vb, ib = orc.row_bytes(4096, n_keep)
+        P = 4096 // 4 * n_keep
+        original = P * (4 + 16) / 8
+        assert (vb + ib) / original == pytest.approx(ratio, abs=0)
+
+
+# ---------------------------------------------------------------------------
+# O5 matvec: closed forms, exact rational brute force, library matmul.
+# ---------------------------------------------------------------------------
+
+def _packed(orc, seed, rows, cols, n_keep, group):
+    return orc.pack(synth.weight_outliers(seed, rows, cols), n_keep, group)
+
+
+def test_matvec_all_ones_is_row_sum(orc):
+    p = _packed(orc, 51, 9, 256, 2, 64)
+    dq = orc.dequant(p)
+    y = orc.matvec(p, np.ones((1, 256), np.float16))
+    want = [math.fsum(row) for row in dq]
+    assert np.allclose(y[0], want, rtol=1e-15, atol=1e-15)
+
+
+def test_matvec_one_hot_is_column(orc):
+    p = _packed(orc, 52, 7, 128, 1, 64)
+    dq = orc.dequant(p)
+    for c in (0, 1, 63, 64, 127):
+        x = np.zeros((1, 128), np.float16)
+        x[0, c] = 1.0
+        assert np.array_equal(orc.matvec(p, x)[0], dq[:, c])
+
+
+def test_matvec_exact_rational(orc):
+    p = _packed(orc, 53, 4, 64, 2, 64)
+    x = synth.activations(9, 3, 64)
+    y = orc.matvec(p, x)
+    xs = x.astype(np.float64)
+    for r in range(4):
+        # exact value from the raw bits: Fractions of (q - z) * s * x
+        pos, q = orc.decode(p.vals[r:r + 1], p.idx[r:r + 1], 1, 64, 2)
+        s = Fraction(orc.f16_bits_to_f64(p.scale[r, 0]))
+        z = Fraction(orc.f16_bits_to_f64(p.zero[r, 0]))
+        for m in range(3):
+            exact = Fraction(0)
+            for j in range(32):
+                c = 4 * (j // 2) + int(pos[0, j])
+                exact += (int(q[0, j]) - z) * s * Fraction(float(xs[m, c]))
+            # 32 rounded fp64 additions: relative error far below 1e-13
+            assert abs(Fraction(y[m, r]) - exact) <= abs(exact) * Fraction(1, 10 ** 13) + Fraction(1, 10 ** 300)
+
+
+def test_matvec_matches_torch_fp64(orc):
+    torch = pytest.importorskip("torch")
+    p = _packed(orc, 54, 33, 512, 2, 128)
+    x = synth.activations(10, 5, 512)
+    y = orc.matvec(p, x)
+    ref = (torch.from_numpy(x.astype(np.float64))
+           @ torch.from_numpy(orc.dequant(p)).T).numpy()
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_matvec_row_subset(orc):
+    p = _packed(orc, 55, 12, 256, 1, 64)
+    x = synth.activations(11, 2, 256)
+    full = orc.matvec(p, x)
+    rows = np.array([11, 0, 5], dtype=np.int64)
+    assert np.array_equal(orc.matvec(p, x, rows), full[:, rows])
+
+
+def test_empty_shapes(orc):
+    p = orc.pack(np.zeros((0, 128), np.float32), 2, 64)
+    assert p.vals.shape == (0, 32)
+    p0 = orc.pack(np.zeros((3, 0), np.float32), 2, 64)
+    y = orc.matvec(p0, np.zeros((1, 0), np.float16))
+    assert y.shape == (1, 3) and not y.any()
