@@ -1,0 +1,534 @@
+"""SparseGemv benchmark: achieved HBM GB/s and us/call at M = 1.
+
+Workload (default): the 7B-style decoder layer set -- q, k, v, o 4096x4096,
+gate, up 11008x4096, down 4096x11008 -- each matrix N:4 pruned and INT4
+group-quantised with a seeded per-matrix (N, g), x one binary16 row.  One
+step = the seven SparseGemv calls of one decode step.  Weights are
+synthetic and seeded (the paper's model is not public).
+
+Timing: W warm-up steps, then exactly K steps, as CUDA graphs replayed on
+one stream, bracketed by a barrier + device synchronisation; CUDA events
+on that stream give the duration; steps rotate over enough distinct copies
+of the packed weights (> 4x the L2 size) that no weight byte is served
+from L2.  value = algorithmic bytes of all steps on all ranks / max time.
+
+Prints one JSON line on rank 0.  --impl reference times the CPU oracle on
+a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "SparseGemv achieved HBM GB/s and us/call (M=1) vs 8 TB/s roofline"
+WORKLOAD = ("7B decoder layer set, M=1: q,k,v,o 4096x4096; gate,up 11008x4096; "
+            "down 4096x11008; seeded per-matrix (N:4, group)")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: no collective on the data path)
+# ---------------------------------------------------------------------------
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v: float, world: int, device=None) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks: NVML polled from a thread during the timed region
+# ---------------------------------------------------------------------------
+
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting",
+            0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sync_boost",
+            0x40: "sw_thermal_slowdown", 0x80: "hw_thermal_slowdown",
+            0x100: "hw_power_brake_slowdown", 0x200: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Reads SM clock and clock-event reasons (read-only NVML queries)."""
+
+    def __init__(self, index: int, period_s: float = 0.001):
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        self._stop = threading.Event()
+        self._thr = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+                return
+            self._nv, self._h = nv, h
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _read(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        self._nv.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(c))
+        fn = getattr(self._nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(self._h, ctypes.byref(r))
+        return c.value, r.value
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self.samples.append(self._read())
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._thr = threading.Thread(target=self._loop, daemon=True)
+            self._thr.start()
+
+    def stop(self):
+        if self._thr:
+            self._stop.set()
+            self._thr.join()
+            self.samples.append(self._read())
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "source": "unavailable"}
+        mhz = [s[0] for s in self.samples]
+        reasons = set()
+        for _, bits in self.samples:
+            for b, name in _REASONS.items():
+                if bits & b:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(mhz),
+                "source": "nvml poll ~1 ms during the timed region"}
+
+
+# ---------------------------------------------------------------------------
+# the workload
+# ---------------------------------------------------------------------------
+
+def workload(seed: int = 0):
+    return synth.config3(seed)
+
+
+def step_bytes(gvs, m=1):
+    return sum(g.bytes(m) for g in gvs)
+
+
+def read_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback 6.8 TB/s"
+
+
+def read_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes from a committed ncu summary, or None if the
+    summary is missing or was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel_tag)
+    if not ent:
+        return None
+    from sparse_weight_only_gb300.build import _stamp
+    if ent.get("source_stamp") != _stamp():
+        return None
+    return ent
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline key)
+# ---------------------------------------------------------------------------
+
+def oracle_time(packed, budget_s: float, min_rows: int = 1):
+    """Times the oracle's matvec on whole row blocks of every matrix until
+    `budget_s` has elapsed.  Returns (bytes, seconds, rows_done)."""
+    import oracle
+    total_b, total_t, rows_done = 0, 0.0, 0
+    nmat = len(packed)
+    i = 0
+    while True:
+        gv, p, x = packed[i % nmat]
+        nr = max(min_rows, gv.rows // 64)
+        start = (i // nmat * nr) % max(gv.rows - nr + 1, 1)
+        rows = np.arange(start, start + nr, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.matvec(p, x, rows)
+        total_t += time.perf_counter() - t0
+        frac = nr / gv.rows
+        total_b += frac * gv.packed_bytes() + 2 * gv.cols + 2 * nr
+        rows_done += nr
+        i += 1
+        if total_t >= budget_s and i >= nmat:
+            break
+    return total_b, total_t, rows_done
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    gvs = workload(args.seed)
+    packed = []
+    for gv in gvs:
+        W = gv.weight()
+        packed.append((gv, oracle.pack(W, gv.n_keep, gv.group), gv.x(1)))
+        del W
+    # each step: one row block (1/64 of the rows) of one matrix, rotating;
+    # the whole W + K run is bounded to about two minutes
+    per_step = max(0.0005, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_time(packed, 0.0)
+    b, t, rows = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        bb, tt, rr = oracle_time(packed, per_step)
+        b, t, rows = b + bb, t + tt, rows + rr
+    gbs = b / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "m": 1, "seed": args.seed},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} rows in row blocks of 1/64 of each matrix, "
+                                   "single-threaded fp64 dequantise + naive matvec"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local):
+    import torch
+    import sparse_weight_only_gb300 as swo
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    swo.build()
+    swo.load()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    m = 1
+
+    gvs = workload(args.seed)
+    t_pack = time.perf_counter()
+    base = []
+    for gv in gvs:
+        W = gv.weight()
+        h = swo.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group, max_m=m,
+                           device=local)
+        h.pack(W)
+        del W
+        base.append(h)
+    t_pack = time.perf_counter() - t_pack
+    canon = [h.export_canonical() for h in base]
+
+    sb = step_bytes(gvs, m)
+    wbytes = sum(g.packed_bytes() for g in gvs)
+    copies = max(2, math.ceil(4 * l2 / wbytes) + 1)
+    sets = [base]
+    for _ in range(copies - 1):
+        cp = []
+        for gv, c in zip(gvs, canon):
+            h = swo.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group, max_m=m,
+                               device=local)
+            h.import_canonical(*c)
+            cp.append(h)
+        sets.append(cp)
+
+    xs = [torch.from_numpy(gv.x(m)).to(dev) for gv in gvs]
+    ys = [torch.empty((m, gv.rows), dtype=torch.float16, device=dev) for gv in gvs]
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+
+    def launch_step(k):
+        for h, x, y in zip(sets[k % copies], xs, ys):
+            h.run(x, y, sptr)
+
+    def capture(nsteps, first):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(nsteps):
+                    launch_step(first + k)
+        return g
+
+    # graphs: a block of `copies` steps (each copy once) and a remainder
+    block = copies
+    with torch.cuda.stream(stream):
+        for k in range(2):
+            launch_step(k)            # eager warm-up before capture
+    torch.cuda.synchronize()
+    g_block = capture(block, 0)
+
+    def replay(nsteps, rem_graphs):
+        q, r = divmod(nsteps, block)
+        for _ in range(q):
+            g_block.replay()
+        if r:
+            rem_graphs[r].replay()
+
+    rem = {}
+    for n in {args.steps % block, args.warmup % block} - {0}:
+        rem[n] = capture(n, 0)
+
+    with torch.cuda.stream(stream):
+        replay(args.warmup, rem)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        replay(args.steps, rem)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(world)
+    t_local = e0.elapsed_time(e1) / 1e3
+    t_max = max_over_ranks(t_local, world, dev)
+    total_bytes = sum_over_ranks(sb * args.steps, world, dev)
+    value = total_bytes / t_max / 1e9
+    ms_step = 1e3 * t_max / args.steps
+    launches = len(gvs) * args.steps
+
+    # correctness of what was timed: all copies produce identical y
+    y_check = [y.clone() for y in ys]
+    with torch.cuda.stream(stream):
+        launch_step(1)
+    torch.cuda.synchronize()
+    same = all(torch.equal(a, b) for a, b in zip(y_check, ys))
+
+    # per-matrix times (same rotation, one matrix at a time, graphs)
+    per = []
+    for i, gv in enumerate(gvs):
+        gi = torch.cuda.CUDAGraph()
+        reps = 4 * copies
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gi, stream=stream):
+                for k in range(reps):
+                    sets[k % copies][i].run(xs[i], ys[i], sptr)
+        gi.replay()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a0.record(stream)
+            for _ in range(5):
+                gi.replay()
+            a1.record(stream)
+        torch.cuda.synchronize()
+        us = a0.elapsed_time(a1) * 1e3 / (5 * reps)
+        per.append({"name": gv.name, "shape": [gv.rows, gv.cols],
+                    "n_keep": gv.n_keep, "group": gv.group,
+                    "bytes": gv.bytes(m), "us": round(us, 3),
+                    "gbs": round(gv.bytes(m) / us / 1e3, 1)})
+        del gi
+
+    # dense fp16 GEMV baseline (cuBLAS via torch), same shapes and rotation
+    dense_us = None
+    try:
+        dense_bytes = sum(2 * g.rows * g.cols for g in gvs)
+        dcopies = max(2, math.ceil(4 * l2 / dense_bytes) + 1)
+        dws = [[torch.randn(g.rows, g.cols, device=dev, dtype=torch.float16)
+                for g in gvs] for _ in range(dcopies)]
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for k in range(2):
+                for w, x in zip(dws[k % dcopies], xs):
+                    torch.nn.functional.linear(x, w)
+            with torch.cuda.graph(gd, stream=stream):
+                for k in range(dcopies * 2):
+                    for w, x, y in zip(dws[k % dcopies], xs, ys):
+                        torch.matmul(x, w.t(), out=y)
+        gd.replay()
+        torch.cuda.synchronize()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            d0.record(stream)
+            for _ in range(5):
+                gd.replay()
+            d1.record(stream)
+        torch.cuda.synchronize()
+        dense_us = d0.elapsed_time(d1) * 1e3 / (5 * dcopies * 2)
+        del dws, gd
+    except Exception as exc:  # pragma: no cover - reported, not fatal
+        dense_us = f"failed: {exc}"
+
+    # end to end through the public host-buffer call: H2D x, kernels, D2H y
+    xh = [torch.from_numpy(gv.x(m)).pin_memory() for gv in gvs]
+    yh = [torch.empty((m, gv.rows), dtype=torch.float16).pin_memory() for gv in gvs]
+    lib = swo.load()
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step(k):
+        for h, x, y in zip(sets[k % copies], xh, yh):
+            rc = lib.sgemv_run_host(h.handle, x.data_ptr(), y.data_ptr(), m, sptr)
+            if rc:
+                raise RuntimeError(lib.sgemv_last_error().decode())
+        stream.synchronize()
+        return float(yh[0][0, 0])
+
+    for k in range(3):
+        e2e_step(k)
+    barrier(world)
+    t0 = time.perf_counter()
+    for k in range(e2e_steps):
+        e2e_step(k)
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = sum_over_ranks(sb * e2e_steps, world, dev) / t_e2e / 1e9
+
+    # CPU oracle on the host cores (rank 0 only), ~10 s bounded sample
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        from oracle import Packed
+        packed = []
+        for gv, c in zip(gvs, canon):
+            packed.append((gv, Packed(gv.rows, gv.cols, gv.n_keep, gv.group, *c),
+                           gv.x(m)))
+        b, t, rows = oracle_time(packed, args.cpu_seconds)
+        cpu = {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{rows} rows of the layer set in blocks of 1/64 of a "
+                         f"matrix, {t:.1f} s single-threaded"}
+
+    peak, peak_src = read_peak()
+    traffic = read_traffic("sgemv_layerset_m1")
+    achieved = sb / (t_local / args.steps) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "us_per_call": 1e3 * ms_step / len(gvs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD, "m": m, "seed": args.seed,
+            "matrices": [[g.name, g.rows, g.cols, f"{g.n_keep}:4", g.group]
+                         for g in gvs],
+            "bytes_per_step": sb,
+            "l2": f"inputs larger than L2: rotation over {copies} packed copies "
+                  f"({copies * wbytes / 1e6:.0f} MB > 4 x L2 {l2 / 1e6:.0f} MB)",
+            "parallelism": f"replicas x{world}",
+            "timing": "CUDA graphs on one stream, CUDA events",
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src,
+                     "traffic": traffic["bytes_per_step"] if traffic else None},
+        "e2e": {"value": e2e, "unit": "GB/s",
+                "h2d_bytes_per_step": sum(2 * m * g.cols for g in gvs),
+                "d2h_bytes_per_step": sum(2 * m * g.rows for g in gvs),
+                "api": "sgemv_run_host per matrix + stream sync per step"},
+        "cpu_baseline": cpu,
+        "clocks": clocks.summary(),
+        "gpu_launches": launches,
+        "per_matrix": per,
+        "dense_fp16_us_per_step": dense_us,
+        "speedup_vs_dense_fp16": (dense_us / (1e3 * ms_step)
+                                  if isinstance(dense_us, float) else None),
+        "pack_seconds": round(t_pack, 3),
+        "copies_identical_y": same,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_init()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

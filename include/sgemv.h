@@ -1,0 +1,163 @@
+/*
+ * sgemv.h -- C ABI of libsgemv: mixed-precision SparseGemv y = W_hat . x on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (Dong et al., "Efficient LLM ad generation via model
+ * compression and parallel verification", arXiv 2605.11582):
+ *   - W is a linear layer's weight, rows x cols (out features x in
+ *     features), pruned N:4 along cols -- 2:4 for critical layers, 1:4 for
+ *     the rest (section 3.2, "Sparsification"; Figure 1 caption);
+ *   - kept weights are quantised to INT4 group-wise with a per-layer group
+ *     size (section 1, "Our core idea"; section 3.2, "Adaptive group
+ *     quantization"), asymmetric with binary16 scale and zero per group;
+ *   - the sparse weight is held in the index-compressed 2bit-CSR form, one
+ *     2-bit in-quad position per kept weight (section 1, contribution 1);
+ *   - the product is an INT4 weight-only GEMV with mixed sparsity, x and y
+ *     in binary16, fp32 accumulation (section 1, contribution 2; section
+ *     3.3).
+ * Pruning keeps the N largest |w| of each quad (Eq. 3 with equal input
+ * norms and no gradient term; ties go to the lower column).  Quantisation
+ * per (row, group of g columns) over the kept values S:
+ *   lo = min(0, min S), hi = max(0, max S);
+ *   s = binary16((hi - lo) / 15) (1.0 if hi == lo; 2^-24 if it rounds to 0);
+ *   z = clamp(rint(-lo / s), 0, 15);  q = clamp(rint(w / s) + z, 0, 15);
+ *   W_hat = (q - z) * s.  All rounding is to nearest, ties to even.
+ *
+ * Canonical 2bit-CSR bytes (the import/export format; P = cols*N/4 kept
+ * weights per row, kept weight j lies in quad floor(j/N), positions ascend
+ * within a quad):
+ *   vals : rows x (P/2) bytes, INT4 code of kept j in byte j/2, low nibble
+ *          for even j;
+ *   idx  : rows x (P/4) bytes, 2-bit position of kept j at bits 2*(j%4) of
+ *          byte j/4;
+ *   scale, zero : rows x (cols/g) binary16 bit patterns, row-major.
+ * On the device the library keeps its own layout of the same information
+ * (see sgemv_sizes); export returns the canonical bytes exactly.
+ *
+ * Conventions for every call:
+ *   - the return value is SGEMV_OK (0) or a negative SGEMV_ERR_* code, and
+ *     sgemv_last_error() then describes the failure (thread-local text);
+ *   - argument errors are detected on the host before anything is launched;
+ *   - device pointers (x_dev, y_dev, w_dev) are owned by the caller and must
+ *     be on the handle's device; host pointers are owned by the caller and
+ *     only read (inputs) or written (outputs) during the call, except for
+ *     sgemv_run_host, whose buffers must stay valid until the stream reaches
+ *     the end of the call's work;
+ *   - a stream argument is a cudaStream_t passed as void*; NULL means the
+ *     legacy default stream;
+ *   - a handle is not safe for concurrent pack/import/export/destroy; any
+ *     number of sgemv_run calls may run concurrently on different streams
+ *     (they only read the packed weight).
+ */
+#ifndef SGEMV_H
+#define SGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sgemv_ctx* sgemv_t;
+
+enum {
+  SGEMV_OK = 0,
+  SGEMV_ERR_ARG = -1,         /* bad argument: shape, pointer, alignment, m */
+  SGEMV_ERR_UNSUPPORTED = -2, /* valid request this build does not support */
+  SGEMV_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+  SGEMV_ERR_STATE = -4,       /* run/export before pack or import */
+  SGEMV_ERR_TIMEOUT = -5,     /* a bounded device-side wait gave up */
+  SGEMV_ERR_NONFINITE = -6,   /* NaN or Inf in the weight given to pack */
+  SGEMV_ERR_RANGE = -7        /* a group's scale does not fit binary16 */
+};
+
+/* Size limits of one handle. */
+#define SGEMV_MAX_ROWS (1 << 24)
+#define SGEMV_MAX_COLS (1 << 20)
+#define SGEMV_MAX_M 64
+
+/*
+ * Create a handle for a rows x cols weight with N = n_keep (1 or 2) kept per
+ * quad and group size `group` (64, 128 or 256 dense columns; cols must be a
+ * multiple of it).  rows and cols may be 0 (empty products).  max_m (1..64)
+ * bounds the activation rows of later runs.  `device` is the CUDA ordinal.
+ * Allocates the packed-weight buffers on that device; nothing is packed yet.
+ * On failure *out is set to NULL.
+ */
+int sgemv_create(sgemv_t* out, int rows, int cols, int n_keep, int group,
+                 int max_m, int device);
+
+/*
+ * Prune, quantise and pack a dense fp32 weight (rows x cols, row-major,
+ * host memory, read only).  The work runs on the handle's device; the call
+ * returns when it is done.  NaN/Inf anywhere -> SGEMV_ERR_NONFINITE; a scale
+ * beyond binary16 -> SGEMV_ERR_RANGE; the handle is then left unpacked.
+ */
+int sgemv_pack(sgemv_t h, const float* w_host);
+
+/* As sgemv_pack, with the dense weight already in device memory; the work is
+ * ordered on `stream`, and the call waits for it before returning. */
+int sgemv_pack_device(sgemv_t h, const float* w_dev, void* stream);
+
+/*
+ * Load canonical 2bit-CSR bytes (host memory, layout above; the byte counts
+ * are those reported by sgemv_sizes).  For N = 2 the two positions of each
+ * quad must ascend strictly (SGEMV_ERR_ARG otherwise).  Synchronous.
+ */
+int sgemv_import(sgemv_t h, const uint8_t* vals, const uint8_t* idx,
+                 const uint16_t* scale, const uint16_t* zero);
+
+/* Write the packed weight back as canonical bytes into host buffers of the
+ * sizes reported by sgemv_sizes.  Synchronous. */
+int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
+                 uint16_t* zero);
+
+/*
+ * y = W_hat . x for m activation rows (0 <= m <= max_m):
+ *   x_dev : m x cols binary16, row-major, 16-byte aligned, device memory;
+ *   y_dev : m x rows binary16, row-major, 2-byte aligned, device memory,
+ *           fully overwritten; must not overlap x_dev;
+ *   accumulation is fp32, each y element rounded once to binary16.
+ * Asynchronous on `stream`: returns after the launch, reporting argument
+ * and launch errors only.  The handle must have been packed or imported.
+ */
+int sgemv_run(sgemv_t h, const void* x_dev, void* y_dev, int m, void* stream);
+
+/*
+ * The same product with x and y in host memory: the call copies x to a
+ * staging buffer owned by the handle, runs, and copies y back, all ordered
+ * on `stream`; it returns without waiting, so the caller synchronises the
+ * stream before reading y_host.  Page-locked host buffers make the copies
+ * asynchronous.  Calls on one handle share its staging buffers and must be
+ * ordered on one stream.
+ */
+int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
+                   void* stream);
+
+/* Synchronise the device, then return and clear the handle's device error
+ * word (SGEMV_OK if no kernel reported an error since the last call). */
+int sgemv_status(sgemv_t h);
+
+/*
+ * Byte counts of the canonical arrays and of the device-resident packed
+ * weight.  Any output pointer may be NULL.
+ */
+int sgemv_sizes(sgemv_t h, size_t* vals_bytes, size_t* idx_bytes,
+                size_t* n_groups, size_t* device_bytes);
+
+/* Algorithmic packed-weight bytes: INT4 values + 2-bit positions + binary16
+ * scale and zero per group (0 for a NULL handle). */
+size_t sgemv_packed_bytes(sgemv_t h);
+
+/* Text of the calling thread's last error ("" if none). */
+const char* sgemv_last_error(void);
+
+/* Free the handle and its device buffers.  NULL is accepted. */
+int sgemv_destroy(sgemv_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMV_H */

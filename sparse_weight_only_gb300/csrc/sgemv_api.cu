@@ -1,0 +1,396 @@
+// sgemv_api.cu -- the extern "C" boundary of libsgemv (declared in
+// include/sgemv.h): argument checks, handle and device-buffer management,
+// host<->device transfers, and kernel dispatch.  No arithmetic of the
+// method happens here; every step of pack and run executes in the CUDA
+// kernels of sgemv_format.cu, sgemv_generic.cu and sgemv_m1.cu.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "sgemv_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(SGEMV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(expr, what)                       \
+  do {                                             \
+    cudaError_t e_ = (expr);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// Makes the handle's device current for the scope and restores the caller's.
+struct DeviceGuard {
+  int prev = -1;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int dev) {
+    err = cudaGetDevice(&prev);
+    if (err == cudaSuccess && prev != dev) err = cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+// A device buffer freed on scope exit (used for pack / import / export
+// temporaries).
+struct DevBuf {
+  void* p = nullptr;
+  ~DevBuf() {
+    if (p) cudaFree(p);
+  }
+  cudaError_t alloc(size_t n) { return n ? cudaMalloc(&p, n) : cudaSuccess; }
+};
+
+sgemv::Layout make_layout(int rows, int cols, int n_keep, int group) {
+  sgemv::Layout L;
+  L.rows = rows;
+  L.cols = cols;
+  L.n_keep = n_keep;
+  L.group = group;
+  L.kept = (int64_t)cols / 4 * n_keep;
+  L.chunks = (L.kept + sgemv::kChunkKept - 1) / sgemv::kChunkKept;
+  L.ngroups = cols / group;
+  L.vals_row = (L.kept + 1) / 2;
+  L.idx_row = (L.kept + 3) / 4;
+  return L;
+}
+
+int check_handle(sgemv_t h) {
+  if (!h) return fail(SGEMV_ERR_ARG, "null handle");
+  return SGEMV_OK;
+}
+
+int dev_err_to_status(int word) {
+  switch (word) {
+    case 0: return SGEMV_OK;
+    case sgemv::kDevErrNonfinite:
+      return fail(SGEMV_ERR_NONFINITE, "weight holds NaN or Inf");
+    case sgemv::kDevErrRange:
+      return fail(SGEMV_ERR_RANGE, "a group's scale does not fit binary16");
+    case sgemv::kDevErrBadIndex:
+      return fail(SGEMV_ERR_ARG, "2:4 positions must ascend strictly within a quad");
+    default:
+      return fail(SGEMV_ERR_CUDA, "device error word %d", word);
+  }
+}
+
+// Reads and clears the error word after the handle's private stream drains.
+int collect_dev_err(sgemv_t h) {
+  CUDA_TRY(cudaStreamSynchronize(h->stream), "cudaStreamSynchronize");
+  int word = 0;
+  CUDA_TRY(cudaMemcpy(&word, h->d_err, sizeof word, cudaMemcpyDeviceToHost),
+           "read error word");
+  CUDA_TRY(cudaMemset(h->d_err, 0, sizeof(int)), "clear error word");
+  return dev_err_to_status(word);
+}
+
+size_t vals_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.chunks * 16; }
+size_t idx_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.chunks * 8; }
+size_t sz_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.ngroups * 4; }
+
+void free_ctx(sgemv_t h) {
+  if (!h) return;
+  cudaFree(h->d_vals);
+  cudaFree(h->d_idx);
+  cudaFree(h->d_sz);
+  cudaFree(h->d_xstage);
+  cudaFree(h->d_ystage);
+  cudaFree(h->d_err);
+  if (h->stream) cudaStreamDestroy(h->stream);
+  delete h;
+}
+
+int pack_on_device(sgemv_t h, const float* w_dev, cudaStream_t s) {
+  const sgemv::Layout& L = h->L;
+  h->ready = false;
+  CUDA_TRY(cudaMemsetAsync(h->d_err, 0, sizeof(int), s), "clear error word");
+  if (vals_dev_bytes(L))
+    CUDA_TRY(cudaMemsetAsync(h->d_vals, 0, vals_dev_bytes(L), s), "memset vals");
+  if (idx_dev_bytes(L))
+    CUDA_TRY(cudaMemsetAsync(h->d_idx, 0, idx_dev_bytes(L), s), "memset idx");
+  CUDA_TRY(sgemv::launch_pack(L, w_dev, h->d_vals, h->d_idx, h->d_sz, h->d_err, s),
+           "pack kernel");
+  CUDA_TRY(cudaStreamSynchronize(s), "pack");
+  int word = 0;
+  CUDA_TRY(cudaMemcpy(&word, h->d_err, sizeof word, cudaMemcpyDeviceToHost),
+           "read error word");
+  CUDA_TRY(cudaMemset(h->d_err, 0, sizeof(int)), "clear error word");
+  int rc = dev_err_to_status(word);
+  if (rc == SGEMV_OK) h->ready = true;
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sgemv_last_error(void) { return g_err; }
+
+int sgemv_create(sgemv_t* out, int rows, int cols, int n_keep, int group,
+                 int max_m, int device) {
+  if (!out) return fail(SGEMV_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  if (rows < 0 || rows > SGEMV_MAX_ROWS)
+    return fail(SGEMV_ERR_ARG, "rows=%d outside [0, %d]", rows, SGEMV_MAX_ROWS);
+  if (cols < 0 || cols > SGEMV_MAX_COLS)
+    return fail(SGEMV_ERR_ARG, "cols=%d outside [0, %d]", cols, SGEMV_MAX_COLS);
+  if (n_keep != 1 && n_keep != 2)
+    return fail(SGEMV_ERR_ARG, "n_keep=%d: only 1:4 and 2:4 are defined", n_keep);
+  if (group != 64 && group != 128 && group != 256)
+    return fail(SGEMV_ERR_ARG, "group=%d: must be 64, 128 or 256", group);
+  if (cols % group != 0)
+    return fail(SGEMV_ERR_ARG, "cols=%d is not a multiple of group=%d", cols, group);
+  if (max_m < 1 || max_m > SGEMV_MAX_M)
+    return fail(SGEMV_ERR_ARG, "max_m=%d outside [1, %d]", max_m, SGEMV_MAX_M);
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device < 0 || device >= ndev)
+    return fail(SGEMV_ERR_ARG, "device=%d but %d device(s) visible", device, ndev);
+  DeviceGuard g(device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+
+  sgemv_t h = new sgemv_ctx();
+  memset(h, 0, sizeof *h);
+  h->L = make_layout(rows, cols, n_keep, group);
+  h->max_m = max_m;
+  h->device = device;
+  h->ready = false;
+  auto try_alloc = [&](void** p, size_t n, const char* what) -> int {
+    if (n == 0) return SGEMV_OK;
+    cudaError_t err = cudaMalloc(p, n);
+    if (err != cudaSuccess) return cuda_fail(err, what);
+    return SGEMV_OK;
+  };
+  int rc = SGEMV_OK;
+  if (!rc) rc = try_alloc((void**)&h->d_vals, vals_dev_bytes(h->L), "cudaMalloc vals");
+  if (!rc) rc = try_alloc((void**)&h->d_idx, idx_dev_bytes(h->L), "cudaMalloc idx");
+  if (!rc) rc = try_alloc((void**)&h->d_sz, sz_dev_bytes(h->L), "cudaMalloc scale/zero");
+  if (!rc) rc = try_alloc((void**)&h->d_xstage, (size_t)max_m * cols * 2, "cudaMalloc x staging");
+  if (!rc) rc = try_alloc((void**)&h->d_ystage, (size_t)max_m * rows * 2, "cudaMalloc y staging");
+  if (!rc) rc = try_alloc((void**)&h->d_err, sizeof(int), "cudaMalloc error word");
+  if (!rc) {
+    e = cudaMemset(h->d_err, 0, sizeof(int));
+    if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemset");
+  }
+  if (!rc) {
+    e = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) rc = cuda_fail(e, "cudaStreamCreate");
+  }
+  if (rc) {
+    free_ctx(h);
+    return rc;
+  }
+  *out = h;
+  return SGEMV_OK;
+}
+
+int sgemv_destroy(sgemv_t h) {
+  if (!h) return SGEMV_OK;
+  DeviceGuard g(h->device);
+  free_ctx(h);
+  return SGEMV_OK;
+}
+
+int sgemv_pack(sgemv_t h, const float* w_host) {
+  if (int rc = check_handle(h)) return rc;
+  const sgemv::Layout& L = h->L;
+  const size_t n = (size_t)L.rows * L.cols;
+  if (n && !w_host) return fail(SGEMV_ERR_ARG, "w_host is NULL");
+  DeviceGuard g(h->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  DevBuf w;
+  CUDA_TRY(w.alloc(n * sizeof(float)), "cudaMalloc dense weight");
+  if (n)
+    CUDA_TRY(cudaMemcpyAsync(w.p, w_host, n * sizeof(float), cudaMemcpyHostToDevice,
+                             h->stream),
+             "copy weight to device");
+  return pack_on_device(h, static_cast<const float*>(w.p), h->stream);
+}
+
+int sgemv_pack_device(sgemv_t h, const float* w_dev, void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  const size_t n = (size_t)h->L.rows * h->L.cols;
+  if (n && !w_dev) return fail(SGEMV_ERR_ARG, "w_dev is NULL");
+  if (n && ((uintptr_t)w_dev & 15u))
+    return fail(SGEMV_ERR_ARG, "w_dev must be 16-byte aligned");
+  DeviceGuard g(h->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  return pack_on_device(h, w_dev, static_cast<cudaStream_t>(stream));
+}
+
+int sgemv_import(sgemv_t h, const uint8_t* vals, const uint8_t* idx,
+                 const uint16_t* scale, const uint16_t* zero) {
+  if (int rc = check_handle(h)) return rc;
+  const sgemv::Layout& L = h->L;
+  const size_t nv = (size_t)L.rows * L.vals_row, ni = (size_t)L.rows * L.idx_row;
+  const size_t ns = (size_t)L.rows * L.ngroups;
+  if ((nv && !vals) || (ni && !idx) || (ns && (!scale || !zero)))
+    return fail(SGEMV_ERR_ARG, "a canonical input pointer is NULL");
+  DeviceGuard g(h->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  h->ready = false;
+  DevBuf cv, ci, cs, cz;
+  CUDA_TRY(cv.alloc(nv), "cudaMalloc");
+  CUDA_TRY(ci.alloc(ni), "cudaMalloc");
+  CUDA_TRY(cs.alloc(ns * 2), "cudaMalloc");
+  CUDA_TRY(cz.alloc(ns * 2), "cudaMalloc");
+  cudaStream_t s = h->stream;
+  if (nv) CUDA_TRY(cudaMemcpyAsync(cv.p, vals, nv, cudaMemcpyHostToDevice, s), "copy vals");
+  if (ni) CUDA_TRY(cudaMemcpyAsync(ci.p, idx, ni, cudaMemcpyHostToDevice, s), "copy idx");
+  if (ns) {
+    CUDA_TRY(cudaMemcpyAsync(cs.p, scale, ns * 2, cudaMemcpyHostToDevice, s), "copy scale");
+    CUDA_TRY(cudaMemcpyAsync(cz.p, zero, ns * 2, cudaMemcpyHostToDevice, s), "copy zero");
+  }
+  CUDA_TRY(cudaMemsetAsync(h->d_err, 0, sizeof(int), s), "clear error word");
+  CUDA_TRY(sgemv::launch_canon_to_device(
+               L, (const uint8_t*)cv.p, (const uint8_t*)ci.p, (const uint16_t*)cs.p,
+               (const uint16_t*)cz.p, h->d_vals, h->d_idx, h->d_sz, h->d_err, s),
+           "import kernel");
+  int rc = collect_dev_err(h);
+  if (rc == SGEMV_OK) h->ready = true;
+  return rc;
+}
+
+int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
+                 uint16_t* zero) {
+  if (int rc = check_handle(h)) return rc;
+  if (!h->ready) return fail(SGEMV_ERR_STATE, "export before pack or import");
+  const sgemv::Layout& L = h->L;
+  const size_t nv = (size_t)L.rows * L.vals_row, ni = (size_t)L.rows * L.idx_row;
+  const size_t ns = (size_t)L.rows * L.ngroups;
+  if ((nv && !vals) || (ni && !idx) || (ns && (!scale || !zero)))
+    return fail(SGEMV_ERR_ARG, "a canonical output pointer is NULL");
+  DeviceGuard g(h->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  DevBuf cv, ci, cs, cz;
+  CUDA_TRY(cv.alloc(nv), "cudaMalloc");
+  CUDA_TRY(ci.alloc(ni), "cudaMalloc");
+  CUDA_TRY(cs.alloc(ns * 2), "cudaMalloc");
+  CUDA_TRY(cz.alloc(ns * 2), "cudaMalloc");
+  cudaStream_t s = h->stream;
+  CUDA_TRY(sgemv::launch_device_to_canon(L, h->d_vals, h->d_idx, h->d_sz,
+                                         (uint8_t*)cv.p, (uint8_t*)ci.p,
+                                         (uint16_t*)cs.p, (uint16_t*)cz.p, s),
+           "export kernel");
+  if (nv) CUDA_TRY(cudaMemcpyAsync(vals, cv.p, nv, cudaMemcpyDeviceToHost, s), "copy vals");
+  if (ni) CUDA_TRY(cudaMemcpyAsync(idx, ci.p, ni, cudaMemcpyDeviceToHost, s), "copy idx");
+  if (ns) {
+    CUDA_TRY(cudaMemcpyAsync(scale, cs.p, ns * 2, cudaMemcpyDeviceToHost, s), "copy scale");
+    CUDA_TRY(cudaMemcpyAsync(zero, cz.p, ns * 2, cudaMemcpyDeviceToHost, s), "copy zero");
+  }
+  CUDA_TRY(cudaStreamSynchronize(s), "export");
+  return SGEMV_OK;
+}
+
+static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s) {
+  const sgemv::Layout& L = h->L;
+  sgemv::RunArgs a;
+  a.vals = h->d_vals;
+  a.idx = h->d_idx;
+  a.sz = h->d_sz;
+  a.x = static_cast<const __half*>(x);
+  a.y = static_cast<__half*>(y);
+  a.m = m;
+  if (m == 0 || L.rows == 0) return SGEMV_OK;
+  cudaError_t e = sgemv::launch_m1(L, a, s);
+  if (e == cudaErrorNotSupported) {
+    (void)cudaGetLastError();
+    e = sgemv::launch_generic(L, a, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "SparseGemv launch");
+  return SGEMV_OK;
+}
+
+static int run_args_ok(sgemv_t h, const void* x, const void* y, int m) {
+  if (int rc = check_handle(h)) return rc;
+  if (!h->ready) return fail(SGEMV_ERR_STATE, "run before pack or import");
+  if (m < 0 || m > h->max_m)
+    return fail(SGEMV_ERR_ARG, "m=%d outside [0, max_m=%d]", m, h->max_m);
+  if (m > 0 && h->L.rows > 0) {
+    if (!y) return fail(SGEMV_ERR_ARG, "y is NULL");
+    if (h->L.cols > 0 && !x) return fail(SGEMV_ERR_ARG, "x is NULL");
+  }
+  return SGEMV_OK;
+}
+
+int sgemv_run(sgemv_t h, const void* x_dev, void* y_dev, int m, void* stream) {
+  if (int rc = run_args_ok(h, x_dev, y_dev, m)) return rc;
+  if (x_dev && ((uintptr_t)x_dev & 15u))
+    return fail(SGEMV_ERR_ARG, "x_dev must be 16-byte aligned");
+  if (y_dev && ((uintptr_t)y_dev & 1u))
+    return fail(SGEMV_ERR_ARG, "y_dev must be 2-byte aligned");
+  if (m > 0 && x_dev && y_dev) {
+    const char* xb = static_cast<const char*>(x_dev);
+    const char* yb = static_cast<const char*>(y_dev);
+    const size_t xn = (size_t)m * h->L.cols * 2, yn = (size_t)m * h->L.rows * 2;
+    if (xn && yn && xb < yb + yn && yb < xb + xn)
+      return fail(SGEMV_ERR_ARG, "x and y overlap");
+  }
+  DeviceGuard g(h->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  return run_checked(h, x_dev, y_dev, m, static_cast<cudaStream_t>(stream));
+}
+
+int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
+                   void* stream) {
+  if (int rc = run_args_ok(h, x_host, y_host, m)) return rc;
+  DeviceGuard g(h->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const sgemv::Layout& L = h->L;
+  if (m == 0 || L.rows == 0) return SGEMV_OK;
+  const size_t xn = (size_t)m * L.cols * 2, yn = (size_t)m * L.rows * 2;
+  if (xn)
+    CUDA_TRY(cudaMemcpyAsync(h->d_xstage, x_host, xn, cudaMemcpyHostToDevice, s),
+             "copy x to device");
+  if (int rc = run_checked(h, h->d_xstage, h->d_ystage, m, s)) return rc;
+  CUDA_TRY(cudaMemcpyAsync(y_host, h->d_ystage, yn, cudaMemcpyDeviceToHost, s),
+           "copy y to host");
+  return SGEMV_OK;
+}
+
+int sgemv_status(sgemv_t h) {
+  if (int rc = check_handle(h)) return rc;
+  DeviceGuard g(h->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  CUDA_TRY(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  int word = 0;
+  CUDA_TRY(cudaMemcpy(&word, h->d_err, sizeof word, cudaMemcpyDeviceToHost),
+           "read error word");
+  CUDA_TRY(cudaMemset(h->d_err, 0, sizeof(int)), "clear error word");
+  return dev_err_to_status(word);
+}
+
+int sgemv_sizes(sgemv_t h, size_t* vals_bytes, size_t* idx_bytes,
+                size_t* n_groups, size_t* device_bytes) {
+  if (int rc = check_handle(h)) return rc;
+  const sgemv::Layout& L = h->L;
+  if (vals_bytes) *vals_bytes = (size_t)L.rows * L.vals_row;
+  if (idx_bytes) *idx_bytes = (size_t)L.rows * L.idx_row;
+  if (n_groups) *n_groups = (size_t)L.rows * L.ngroups;
+  if (device_bytes) *device_bytes = vals_dev_bytes(L) + idx_dev_bytes(L) + sz_dev_bytes(L);
+  return SGEMV_OK;
+}
+
+size_t sgemv_packed_bytes(sgemv_t h) {
+  if (!h) return 0;
+  const sgemv::Layout& L = h->L;
+  const size_t kept = (size_t)L.rows * L.kept;
+  return kept / 2 + kept / 4 + (size_t)L.rows * L.ngroups * 4;
+}
+
+}  // extern "C"

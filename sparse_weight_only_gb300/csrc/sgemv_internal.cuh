@@ -1,0 +1,103 @@
+// sgemv_internal.cuh -- handle layout, device layout constants and launch
+// declarations shared by the library's translation units.
+//
+// Device layout of a packed weight (all row-major over rows):
+//   chunk  : 32 consecutive kept weights of one row = 16 "pair units" of two
+//            kept weights each.  A row holds ceil(P / 32) chunks; a tail
+//            chunk is zero-filled past the row's last kept weight.
+//   vals   : 16 bytes per chunk, identical to the canonical nibble order
+//            (kept weight i of the chunk at bits 4*(i%8) of 32-bit word i/8).
+//   idx    : 8 bytes per chunk; pair unit u's 4-bit code at bits 4*(u%8) of
+//            32-bit word u/8.
+//              N = 2: unit u is quad 16*chunk + u; its two ascending
+//                     positions (a, b) are stored as one of six codes,
+//                     kPair24 below;
+//              N = 1: unit u is quads (32*chunk + 2u, 32*chunk + 2u + 1);
+//                     code = a | b << 2 with a, b their positions (this is
+//                     the canonical bit order unchanged).
+//   sz     : 4 bytes per (row, group): binary16 scale in the low half,
+//            binary16 zero in the high half.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sgemv.h"
+
+namespace sgemv {
+
+constexpr int kChunkKept = 32;   // kept weights per chunk
+constexpr int kUnitsPerChunk = 16;
+
+// Six ascending position pairs of a 2:4 quad, in code order.
+// code 0:(0,1) 1:(0,2) 2:(0,3) 3:(1,2) 4:(1,3) 5:(2,3)
+__host__ __device__ constexpr int pair24_a(int code) {
+  return code < 3 ? 0 : (code < 5 ? 1 : 2);
+}
+__host__ __device__ constexpr int pair24_b(int code) {
+  return code == 0 ? 1 : (code == 1 ? 2 : (code == 2 ? 3 : (code == 3 ? 2 : 3)));
+}
+// Inverse: (a | b << 2) -> code, or -1 when a >= b.
+__host__ __device__ constexpr int pair24_code(int a, int b) {
+  return a >= b ? -1 : (a == 0 ? b - 1 : (a == 1 ? b + 1 : 5));
+}
+
+struct Layout {
+  int rows, cols, n_keep, group;
+  int64_t kept;        // P, kept weights per row
+  int64_t chunks;      // chunks per row (device layout)
+  int64_t ngroups;     // cols / group
+  int64_t vals_row;    // canonical bytes per row
+  int64_t idx_row;
+};
+
+}  // namespace sgemv
+
+struct sgemv_ctx {
+  sgemv::Layout L;
+  int max_m;
+  int device;
+  bool ready;
+  uint4* d_vals;       // rows x chunks
+  uint2* d_idx;        // rows x chunks
+  uint32_t* d_sz;      // rows x ngroups
+  __half* d_xstage;    // max_m x cols (sgemv_run_host)
+  __half* d_ystage;    // max_m x rows
+  int* d_err;          // device error word
+  cudaStream_t stream; // private stream for pack / import / export
+};
+
+namespace sgemv {
+
+// Error word values written by kernels (first error wins).
+constexpr int kDevErrNonfinite = 1;
+constexpr int kDevErrRange = 2;
+constexpr int kDevErrBadIndex = 3;
+
+// ---- format kernels (sgemv_format.cu) ----
+cudaError_t launch_pack(const Layout& L, const float* w, uint4* vals, uint2* idx,
+                        uint32_t* sz, int* err, cudaStream_t s);
+cudaError_t launch_canon_to_device(const Layout& L, const uint8_t* cvals,
+                                   const uint8_t* cidx, const uint16_t* scale,
+                                   const uint16_t* zero, uint4* vals, uint2* idx,
+                                   uint32_t* sz, int* err, cudaStream_t s);
+cudaError_t launch_device_to_canon(const Layout& L, const uint4* vals,
+                                   const uint2* idx, const uint32_t* sz,
+                                   uint8_t* cvals, uint8_t* cidx, uint16_t* scale,
+                                   uint16_t* zero, cudaStream_t s);
+
+// ---- product kernels ----
+struct RunArgs {
+  const uint4* vals;
+  const uint2* idx;
+  const uint32_t* sz;
+  const __half* x;
+  __half* y;
+  int m;
+};
+cudaError_t launch_generic(const Layout& L, const RunArgs& a, cudaStream_t s);
+// Returns cudaErrorNotSupported when the fast path does not cover the case.
+cudaError_t launch_m1(const Layout& L, const RunArgs& a, cudaStream_t s);
+
+}  // namespace sgemv
