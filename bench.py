@@ -427,6 +427,12 @@ def run_ours(args, rank, world, local):
     except Exception as exc:  # pragma: no cover - reported, not fatal
         dense_us = f"failed: {exc}"
 
+    # small-M verification batches (beam / prefix-tree nodes): the config-4
+    # layer set, all 2:4 g = 128, x with M rows; bytes and kept-weight flops
+    batch = None
+    if not args.no_batch:
+        batch = run_batch_sweep(args, swo, dev, stream, l2)
+
     # end to end through the public host-buffer call: H2D x, kernels, D2H y
     xh = [torch.from_numpy(gv.x(m)).pin_memory() for gv in gvs]
     yh = [torch.empty((m, gv.rows), dtype=torch.float16).pin_memory() for gv in gvs]
@@ -500,11 +506,74 @@ def run_ours(args, rank, world, local):
         "speedup_vs_dense_fp16": (dense_us / (1e3 * ms_step)
                                   if isinstance(dense_us, float) else None),
         "pack_seconds": round(t_pack, 3),
+        "batch_m": batch,
         "copies_identical_y": same,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_batch_sweep(args, swo, dev, stream, l2):
+    """us and GB/s per M for the config-4 set (seven 2:4 g128 matrices)."""
+    import torch
+    gvs = synth.config4(args.seed)
+    mmax = max(synth.CONFIG4_M)
+    hs0 = []
+    for gv in gvs:
+        W = gv.weight()
+        h = swo.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group, max_m=mmax,
+                           device=dev.index)
+        h.pack(W)
+        del W
+        hs0.append(h)
+    canon = [h.export_canonical() for h in hs0]
+    wbytes = sum(g.packed_bytes() for g in gvs)
+    copies = max(2, math.ceil(4 * l2 / wbytes) + 1)
+    sets = [hs0]
+    for _ in range(copies - 1):
+        cp = []
+        for gv, c in zip(gvs, canon):
+            h = swo.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group, max_m=mmax,
+                               device=dev.index)
+            h.import_canonical(*c)
+            cp.append(h)
+        sets.append(cp)
+    sptr = stream.cuda_stream
+    out = {}
+    for m in synth.CONFIG4_M:
+        xs = [torch.from_numpy(gv.x(m)).to(dev) for gv in gvs]
+        ys = [torch.empty((m, gv.rows), dtype=torch.float16, device=dev) for gv in gvs]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for h, x, y in zip(sets[0], xs, ys):
+                h.run(x, y, sptr)
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(copies):
+                    for h, x, y in zip(sets[k], xs, ys):
+                        h.run(x, y, sptr)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        reps = 5
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+        b = step_bytes(gvs, m)
+        fl = sum(gv.flops(m) for gv in gvs)
+        out[str(m)] = {"us_per_step": round(us, 3), "gbs": round(b / us / 1e3, 1),
+                       "tflops": round(fl / us / 1e6, 2),
+                       "us_per_call": round(us / len(gvs), 3)}
+        del g
+    for st in sets:
+        for h in st:
+            h.close()
+    return out
 
 
 def main(argv=None):
@@ -516,6 +585,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-batch", action="store_true",
+                    help="skip the small-M (config 4) sweep")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

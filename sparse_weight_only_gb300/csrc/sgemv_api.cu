@@ -62,7 +62,9 @@ sgemv::Layout make_layout(int rows, int cols, int n_keep, int group) {
   L.group = group;
   L.kept = (int64_t)cols / 4 * n_keep;
   L.chunks = (L.kept + sgemv::kChunkKept - 1) / sgemv::kChunkKept;
+  L.cstride = (L.chunks + 1) & ~(int64_t)1;
   L.ngroups = cols / group;
+  L.gstride = (L.ngroups + 3) & ~(int64_t)3;
   L.vals_row = (L.kept + 1) / 2;
   L.idx_row = (L.kept + 3) / 4;
   return L;
@@ -97,9 +99,9 @@ int collect_dev_err(sgemv_t h) {
   return dev_err_to_status(word);
 }
 
-size_t vals_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.chunks * 16; }
-size_t idx_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.chunks * 8; }
-size_t sz_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.ngroups * 4; }
+size_t vals_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.cstride * 16; }
+size_t idx_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.cstride * 8; }
+size_t sz_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.gstride * 4; }
 
 void free_ctx(sgemv_t h) {
   if (!h) return;
@@ -121,6 +123,8 @@ int pack_on_device(sgemv_t h, const float* w_dev, cudaStream_t s) {
     CUDA_TRY(cudaMemsetAsync(h->d_vals, 0, vals_dev_bytes(L), s), "memset vals");
   if (idx_dev_bytes(L))
     CUDA_TRY(cudaMemsetAsync(h->d_idx, 0, idx_dev_bytes(L), s), "memset idx");
+  if (sz_dev_bytes(L))
+    CUDA_TRY(cudaMemsetAsync(h->d_sz, 0, sz_dev_bytes(L), s), "memset scale/zero");
   CUDA_TRY(sgemv::launch_pack(L, w_dev, h->d_vals, h->d_idx, h->d_sz, h->d_err, s),
            "pack kernel");
   CUDA_TRY(cudaStreamSynchronize(s), "pack");
@@ -256,6 +260,8 @@ int sgemv_import(sgemv_t h, const uint8_t* vals, const uint8_t* idx,
     CUDA_TRY(cudaMemcpyAsync(cz.p, zero, ns * 2, cudaMemcpyHostToDevice, s), "copy zero");
   }
   CUDA_TRY(cudaMemsetAsync(h->d_err, 0, sizeof(int), s), "clear error word");
+  if (sz_dev_bytes(L))
+    CUDA_TRY(cudaMemsetAsync(h->d_sz, 0, sz_dev_bytes(L), s), "memset scale/zero");
   CUDA_TRY(sgemv::launch_canon_to_device(
                L, (const uint8_t*)cv.p, (const uint8_t*)ci.p, (const uint16_t*)cs.p,
                (const uint16_t*)cz.p, h->d_vals, h->d_idx, h->d_sz, h->d_err, s),
@@ -306,7 +312,9 @@ static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s)
   a.y = static_cast<__half*>(y);
   a.m = m;
   if (m == 0 || L.rows == 0) return SGEMV_OK;
-  cudaError_t e = sgemv::launch_m1(L, a, s);
+  // m = 1: the CUDA-core decode kernel; 2:4 with m >= 2: the sparse tensor
+  // core kernel; anything else: the general kernel
+  cudaError_t e = m == 1 ? sgemv::launch_m1(L, a, s) : sgemv::launch_mma(L, a, s);
   if (e == cudaErrorNotSupported) {
     (void)cudaGetLastError();
     e = sgemv::launch_generic(L, a, s);

@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict_
   // Device layout: the row's kept weights are contiguous, 32 per 16-byte
   // chunk, in canonical nibble order.  This thread owns kept weights
   // [4N k, 4N (k+1)) of the row.
-  const int64_t vrow = L.chunks * 16;   // device bytes per row (vals)
-  const int64_t irow = L.chunks * 8;    // device bytes per row (idx)
+  const int64_t vrow = L.cstride * 16;  // device bytes per row (vals)
+  const int64_t irow = L.cstride * 8;   // device bytes per row (idx)
   if constexpr (N == 2) {
     uint32_t vw = 0;
     uint32_t iw = 0;
@@ -154,25 +154,26 @@ __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict_
   if ((threadIdx.x & (seg - 1)) == 0) {
     const int64_t G = (16 * k) / L.group;
     const unsigned short z16 = __half_as_ushort(__float2half_rn(zfl));
-    sz[r * L.ngroups + G] = (uint32_t)s16 | ((uint32_t)z16 << 16);
+    sz[r * L.gstride + G] = (uint32_t)s16 | ((uint32_t)z16 << 16);
   }
 }
 
-// Canonical -> device: one thread per (row, chunk).
+// Canonical -> device: one thread per (row, chunk slot in memory); slots
+// past the row's kept weights are written as zeros.
 template <int N>
 __global__ void k_canon_to_device(Layout L, const uint8_t* __restrict__ cvals,
                                   const uint8_t* __restrict__ cidx,
                                   uint8_t* __restrict__ vals,
                                   uint8_t* __restrict__ idx,
                                   int* __restrict__ err) {
-  const int64_t total = (int64_t)L.rows * L.chunks;
+  const int64_t total = (int64_t)L.rows * L.cstride;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= total) return;
-  const int64_t r = t / L.chunks, c = t % L.chunks;
+  const int64_t r = t / L.cstride, c = t % L.cstride;
   const uint8_t* vsrc = cvals + r * L.vals_row;
   const uint8_t* isrc = cidx + r * L.idx_row;
-  uint8_t* vdst = vals + (r * L.chunks + c) * 16;
-  uint8_t* idst = idx + (r * L.chunks + c) * 8;
+  uint8_t* vdst = vals + (r * L.cstride + c) * 16;
+  uint8_t* idst = idx + (r * L.cstride + c) * 8;
   for (int b = 0; b < 16; ++b) {
     const int64_t o = 16 * c + b;
     vdst[b] = o < L.vals_row ? vsrc[o] : 0;
@@ -197,21 +198,24 @@ __global__ void k_canon_to_device(Layout L, const uint8_t* __restrict__ cvals,
   }
 }
 
-__global__ void k_sz_to_device(int64_t n, const uint16_t* __restrict__ scale,
+__global__ void k_sz_to_device(Layout L, const uint16_t* __restrict__ scale,
                                const uint16_t* __restrict__ zero,
                                uint32_t* __restrict__ sz) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) sz[i] = (uint32_t)scale[i] | ((uint32_t)zero[i] << 16);
+  if (i >= (int64_t)L.rows * L.ngroups) return;
+  const int64_t r = i / L.ngroups, G = i % L.ngroups;
+  sz[r * L.gstride + G] = (uint32_t)scale[i] | ((uint32_t)zero[i] << 16);
 }
 
-__global__ void k_sz_to_canon(int64_t n, const uint32_t* __restrict__ sz,
+__global__ void k_sz_to_canon(Layout L, const uint32_t* __restrict__ sz,
                               uint16_t* __restrict__ scale,
                               uint16_t* __restrict__ zero) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) {
-    scale[i] = (uint16_t)(sz[i] & 0xFFFFu);
-    zero[i] = (uint16_t)(sz[i] >> 16);
-  }
+  if (i >= (int64_t)L.rows * L.ngroups) return;
+  const int64_t r = i / L.ngroups, G = i % L.ngroups;
+  const uint32_t w = sz[r * L.gstride + G];
+  scale[i] = (uint16_t)(w & 0xFFFFu);
+  zero[i] = (uint16_t)(w >> 16);
 }
 
 // Device -> canonical: one thread per (row, chunk).
@@ -224,8 +228,8 @@ __global__ void k_device_to_canon(Layout L, const uint8_t* __restrict__ vals,
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= total) return;
   const int64_t r = t / L.chunks, c = t % L.chunks;
-  const uint8_t* vsrc = vals + (r * L.chunks + c) * 16;
-  const uint8_t* isrc = idx + (r * L.chunks + c) * 8;
+  const uint8_t* vsrc = vals + (r * L.cstride + c) * 16;
+  const uint8_t* isrc = idx + (r * L.cstride + c) * 8;
   uint8_t* vdst = cvals + r * L.vals_row;
   uint8_t* idst = cidx + r * L.idx_row;
   for (int b = 0; b < 16; ++b) {
@@ -273,7 +277,7 @@ cudaError_t launch_canon_to_device(const Layout& L, const uint8_t* cvals,
                                    const uint8_t* cidx, const uint16_t* scale,
                                    const uint16_t* zero, uint4* vals, uint2* idx,
                                    uint32_t* sz, int* err, cudaStream_t s) {
-  const int64_t total = (int64_t)L.rows * L.chunks;
+  const int64_t total = (int64_t)L.rows * L.cstride;
   if (total > 0) {
     if (L.n_keep == 2)
       k_canon_to_device<2><<<blocks_for(total, 256), 256, 0, s>>>(
@@ -285,7 +289,7 @@ cudaError_t launch_canon_to_device(const Layout& L, const uint8_t* cvals,
           reinterpret_cast<uint8_t*>(idx), err);
   }
   const int64_t ns = (int64_t)L.rows * L.ngroups;
-  if (ns > 0) k_sz_to_device<<<blocks_for(ns, 256), 256, 0, s>>>(ns, scale, zero, sz);
+  if (ns > 0) k_sz_to_device<<<blocks_for(ns, 256), 256, 0, s>>>(L, scale, zero, sz);
   return cudaGetLastError();
 }
 
@@ -305,7 +309,7 @@ cudaError_t launch_device_to_canon(const Layout& L, const uint4* vals,
           reinterpret_cast<const uint8_t*>(idx), cvals, cidx);
   }
   const int64_t ns = (int64_t)L.rows * L.ngroups;
-  if (ns > 0) k_sz_to_canon<<<blocks_for(ns, 256), 256, 0, s>>>(ns, sz, scale, zero);
+  if (ns > 0) k_sz_to_canon<<<blocks_for(ns, 256), 256, 0, s>>>(L, sz, scale, zero);
   return cudaGetLastError();
 }
 

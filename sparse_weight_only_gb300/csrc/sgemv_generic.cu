@@ -22,9 +22,9 @@ k_generic(Layout L, RunArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (r >= L.rows) return;
-  const uint4* vrow = a.vals + r * L.chunks;
-  const uint2* irow = a.idx + r * L.chunks;
-  const uint32_t* szrow = a.sz + r * L.ngroups;
+  const uint4* vrow = a.vals + r * L.cstride;
+  const uint2* irow = a.idx + r * L.cstride;
+  const uint32_t* szrow = a.sz + r * L.gstride;
 
   for (int m0 = 0; m0 < a.m; m0 += kMTile) {
     float acc[kMTile];

@@ -4,7 +4,9 @@
 // Device layout of a packed weight (all row-major over rows):
 //   chunk  : 32 consecutive kept weights of one row = 16 "pair units" of two
 //            kept weights each.  A row holds ceil(P / 32) chunks; a tail
-//            chunk is zero-filled past the row's last kept weight.
+//            chunk is zero-filled past the row's last kept weight, and the
+//            row's chunk count in memory is rounded up to even (zero chunk)
+//            so that every row of `idx` starts on a 16-byte boundary.
 //   vals   : 16 bytes per chunk, identical to the canonical nibble order
 //            (kept weight i of the chunk at bits 4*(i%8) of 32-bit word i/8).
 //   idx    : 8 bytes per chunk; pair unit u's 4-bit code at bits 4*(u%8) of
@@ -16,7 +18,8 @@
 //                     code = a | b << 2 with a, b their positions (this is
 //                     the canonical bit order unchanged).
 //   sz     : 4 bytes per (row, group): binary16 scale in the low half,
-//            binary16 zero in the high half.
+//            binary16 zero in the high half; rows padded with zero words to
+//            a multiple of 4 groups (16-byte aligned rows).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -46,8 +49,10 @@ __host__ __device__ constexpr int pair24_code(int a, int b) {
 struct Layout {
   int rows, cols, n_keep, group;
   int64_t kept;        // P, kept weights per row
-  int64_t chunks;      // chunks per row (device layout)
+  int64_t chunks;      // chunks holding the row's kept weights
+  int64_t cstride;     // chunks per row in memory: `chunks` rounded up to even
   int64_t ngroups;     // cols / group
+  int64_t gstride;     // scale/zero words per row in memory: multiple of 4
   int64_t vals_row;    // canonical bytes per row
   int64_t idx_row;
 };
@@ -97,7 +102,8 @@ struct RunArgs {
   int m;
 };
 cudaError_t launch_generic(const Layout& L, const RunArgs& a, cudaStream_t s);
-// Returns cudaErrorNotSupported when the fast path does not cover the case.
+// Each returns cudaErrorNotSupported when it does not cover the case.
 cudaError_t launch_m1(const Layout& L, const RunArgs& a, cudaStream_t s);
+cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s);
 
 }  // namespace sgemv

@@ -34,11 +34,24 @@
 namespace sgemv {
 namespace {
 
-constexpr int kNT = 512;           // threads per CTA (one CTA per SM)
+#ifndef SGEMV_M1_NT
+#define SGEMV_M1_NT 512
+#endif
+#ifndef SGEMV_M1_D
+#define SGEMV_M1_D 2
+#endif
+#ifndef SGEMV_M1_MINB
+#define SGEMV_M1_MINB 1
+#endif
+#ifndef SGEMV_M1_GRIDB
+#define SGEMV_M1_GRIDB SGEMV_M1_MINB
+#endif
+constexpr int kNT = SGEMV_M1_NT;   // threads per CTA (one CTA per SM)
 constexpr int kNW = kNT / 32;
-constexpr int kD = 4;              // prefetch depth in chunks
+constexpr int kD = SGEMV_M1_D;     // prefetch depth in chunks
 constexpr int kSmemLimit = 227 * 1024;
 constexpr uint32_t kTabAlign = 2048;
+constexpr int kSmemPerSm = 228 * 1024;
 
 template <int N>
 struct M1Cfg {
@@ -58,9 +71,11 @@ struct M1Params {
   const uint32_t* sz;
   const __half* x;
   __half* y;
-  int rows, cols, ngroups;
+  int rows, cols;
+  int gstride;       // scale/zero words per row in memory
   int gshift;        // log2(group)
-  int chunks;        // per row
+  int chunks;        // chunks holding a row's kept weights
+  int cstride;       // chunks per row in memory
   int rows_per_cta;
   int slice_chunks;  // 32 * cpl
   int nslices;
@@ -89,6 +104,23 @@ __device__ __forceinline__ uint32_t ld_nc4(const uint32_t* p) {
   return v;
 }
 
+// Asks the TMA unit to stage [p, p + bytes) into L2 (a hint: no data
+// returns to the SM).  The range is shrunk to whole 16-byte units inside
+// [lo, hi), the bounds of the buffer it belongs to.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, const void* lo,
+                                            const void* hi) {
+  uintptr_t a = (uintptr_t)p, b = a + bytes;
+  a = (a + 15) & ~(uintptr_t)15;
+  if (a < (uintptr_t)lo) a = ((uintptr_t)lo + 15) & ~(uintptr_t)15;
+  if (b > (uintptr_t)hi) b = (uintptr_t)hi;
+  b &= ~(uintptr_t)15;
+  while (a < b) {
+    const uint32_t n = (uint32_t)min((uintptr_t)65536, b - a);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
+    a += n;
+  }
+}
+
 template <int OFF>
 __device__ __forceinline__ float2 lds_pair(uint32_t addr) {
   float2 v;
@@ -102,10 +134,6 @@ __device__ __forceinline__ void sts_pair(uint32_t addr, float a, float b) {
   asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(addr), "f"(a), "f"(b));
 }
 
-__device__ __forceinline__ float mag(uint32_t bits) {
-  return __uint_as_float(bits | 0x4B000000u);
-}
-
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -113,39 +141,46 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;");
 }
 
-// Subtract constants for one (scale, zero) group: the four f32x2 pairs are
-// -(2^23 + z 2^p) for the classes p of the units' nibbles.
+// Subtract constants for one (scale, zero) group: -(2^23 + z 2^p) for the
+// nibble classes p = (0, 4) and (8, 12).
 struct ZConst {
-  float2 c0, c1, c2, c3;
+  float2 ca, cb;
 };
 
 __device__ __forceinline__ ZConst zconst(float z) {
   const float2 zz = make_float2(z, z);
   const float2 mm = make_float2(-8388608.0f, -8388608.0f);
   ZConst k;
-  k.c0 = __ffma2_rn(zz, make_float2(-1.0f, -16.0f), mm);
-  k.c1 = __ffma2_rn(zz, make_float2(-256.0f, -4096.0f), mm);
-  k.c2 = __ffma2_rn(zz, make_float2(-65536.0f, -256.0f), mm);
-  k.c3 = __ffma2_rn(zz, make_float2(-4096.0f, -65536.0f), mm);
+  k.ca = __ffma2_rn(zz, make_float2(-1.0f, -16.0f), mm);
+  k.cb = __ffma2_rn(zz, make_float2(-256.0f, -4096.0f), mm);
   return k;
 }
 
-// One 32-bit word of nibbles (pair units u0..u0+3) times its x pairs.
-// Nibble classes: n0 2^0, n1 2^4, n2 2^8, n3 2^12, n4 2^16, and after a
-// 12-bit shift n5 2^8, n6 2^12, n7 2^16.
+// 2^23 + q 2^p as a float, from the nibble at bits p..p+3 of v: one LOP3
+// ((v & MASK) | magic) with the exponent pattern held in a register.
+template <uint32_t MASK>
+__device__ __forceinline__ float mag(uint32_t v, uint32_t magic) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "n"(MASK), "r"(magic));
+  return __uint_as_float(r);
+}
+
+// One 32-bit word of nibbles (pair units U0..U0+3, one per byte) times its
+// x pairs.  Bytes 0 and 1 decode in place (classes 2^0,2^4 and 2^8,2^12);
+// bytes 2 and 3 after a 16-bit shift, into the same classes.
 template <int E, int U0, bool FIRST>
 __device__ __forceinline__ void word_fma(uint32_t v, uint32_t codes, uint32_t base,
-                                         const ZConst& k, float2& a0, float2& a1,
-                                         float2& a2, float2& a3) {
-  const uint32_t vs = v >> 12;
-  float2 d0 = make_float2(mag(v & 0xFu), mag(v & 0xF0u));
-  float2 d1 = make_float2(mag(v & 0xF00u), mag(v & 0xF000u));
-  float2 d2 = make_float2(mag(v & 0xF0000u), mag(vs & 0xF00u));
-  float2 d3 = make_float2(mag(vs & 0xF000u), mag(vs & 0xF0000u));
-  d0 = __fadd2_rn(d0, k.c0);
-  d1 = __fadd2_rn(d1, k.c1);
-  d2 = __fadd2_rn(d2, k.c2);
-  d3 = __fadd2_rn(d3, k.c3);
+                                         uint32_t magic, const ZConst& k, float2& a0,
+                                         float2& a1, float2& a2, float2& a3) {
+  const uint32_t vs = v >> 16;
+  float2 d0 = make_float2(mag<0xFu>(v, magic), mag<0xF0u>(v, magic));
+  float2 d1 = make_float2(mag<0xF00u>(v, magic), mag<0xF000u>(v, magic));
+  float2 d2 = make_float2(mag<0xFu>(vs, magic), mag<0xF0u>(vs, magic));
+  float2 d3 = make_float2(mag<0xF00u>(vs, magic), mag<0xF000u>(vs, magic));
+  d0 = __fadd2_rn(d0, k.ca);
+  d1 = __fadd2_rn(d1, k.cb);
+  d2 = __fadd2_rn(d2, k.ca);
+  d3 = __fadd2_rn(d3, k.cb);
   // code of unit U0+s sits at bits 4s of `codes`; table stride 128 B/entry
   const float2 x0 = lds_pair<(U0 + 0) * E * 128>(((codes << 7) & 0x780u) | base);
   const float2 x1 = lds_pair<(U0 + 1) * E * 128>(((codes << 3) & 0x780u) | base);
@@ -164,12 +199,13 @@ __device__ __forceinline__ void word_fma(uint32_t v, uint32_t codes, uint32_t ba
   }
 }
 
-// Removes the 2^p class factors and folds the accumulators into one float.
+// Removes the 2^p class factors and folds the accumulators into one float:
+// a0, a2 hold classes (2^0, 2^4), a1, a3 hold (2^8, 2^12).
 __device__ __forceinline__ float fold(float2 a0, float2 a1, float2 a2, float2 a3) {
-  float2 t = __fmul2_rn(a0, make_float2(1.0f, 0.0625f));
-  t = __ffma2_rn(a1, make_float2(0x1p-8f, 0x1p-12f), t);
-  t = __ffma2_rn(a2, make_float2(0x1p-16f, 0x1p-8f), t);
-  t = __ffma2_rn(a3, make_float2(0x1p-12f, 0x1p-16f), t);
+  const float2 lo = __fadd2_rn(a0, a2);
+  const float2 hi = __fadd2_rn(a1, a3);
+  float2 t = __fmul2_rn(lo, make_float2(1.0f, 0.0625f));
+  t = __ffma2_rn(hi, make_float2(0x1p-8f, 0x1p-12f), t);
   return t.x + t.y;
 }
 
@@ -185,24 +221,25 @@ __device__ __forceinline__ float sz_zero(uint32_t w) {
 // in the first and 8..15 in the second.
 template <int N, bool G2>
 __device__ __forceinline__ float chunk_dot(const uint4& v, const uint2& ix,
-                                           uint32_t sa, uint32_t sb, uint32_t base) {
+                                           uint32_t sa, uint32_t sb, uint32_t base,
+                                           uint32_t magic) {
   constexpr int E = M1Cfg<N>::E;
   float2 a0, a1, a2, a3;
   if (!G2) {
     const ZConst k = zconst(sz_zero(sa));
-    word_fma<E, 0, true>(v.x, ix.x, base, k, a0, a1, a2, a3);
-    word_fma<E, 4, false>(v.y, ix.x >> 16, base, k, a0, a1, a2, a3);
-    word_fma<E, 8, false>(v.z, ix.y, base, k, a0, a1, a2, a3);
-    word_fma<E, 12, false>(v.w, ix.y >> 16, base, k, a0, a1, a2, a3);
+    word_fma<E, 0, true>(v.x, ix.x, base, magic, k, a0, a1, a2, a3);
+    word_fma<E, 4, false>(v.y, ix.x >> 16, base, magic, k, a0, a1, a2, a3);
+    word_fma<E, 8, false>(v.z, ix.y, base, magic, k, a0, a1, a2, a3);
+    word_fma<E, 12, false>(v.w, ix.y >> 16, base, magic, k, a0, a1, a2, a3);
     return sz_scale(sa) * fold(a0, a1, a2, a3);
   } else {
     const ZConst ka = zconst(sz_zero(sa));
-    word_fma<E, 0, true>(v.x, ix.x, base, ka, a0, a1, a2, a3);
-    word_fma<E, 4, false>(v.y, ix.x >> 16, base, ka, a0, a1, a2, a3);
+    word_fma<E, 0, true>(v.x, ix.x, base, magic, ka, a0, a1, a2, a3);
+    word_fma<E, 4, false>(v.y, ix.x >> 16, base, magic, ka, a0, a1, a2, a3);
     const float ya = sz_scale(sa) * fold(a0, a1, a2, a3);
     const ZConst kb = zconst(sz_zero(sb));
-    word_fma<E, 8, true>(v.z, ix.y, base, kb, a0, a1, a2, a3);
-    word_fma<E, 12, false>(v.w, ix.y >> 16, base, kb, a0, a1, a2, a3);
+    word_fma<E, 8, true>(v.z, ix.y, base, magic, kb, a0, a1, a2, a3);
+    word_fma<E, 12, false>(v.w, ix.y >> 16, base, magic, kb, a0, a1, a2, a3);
     return fmaf(sz_scale(sb), fold(a0, a1, a2, a3), ya);
   }
 }
@@ -228,7 +265,7 @@ struct Item {
 };
 
 template <int N, bool G2>
-__global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
+__global__ void __launch_bounds__(kNT, SGEMV_M1_MINB) k_m1(M1Params p) {
   using C = M1Cfg<N>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
@@ -246,11 +283,13 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   const uint32_t lane_base = smem_s + (uint32_t)((lane >> 4) * S) * 128u + (lane & 15) * 8u;
   constexpr uint32_t kChunkSlotBytes = kUnitsPerChunk * C::E * 128;
 
+  uint32_t magic = 0x4B000000u;  // exponent of 2^23, kept in a register
+  asm volatile("" : "+r"(magic));
   const int r0 = blockIdx.x * p.rows_per_cta;
   const int nr = max(0, min(p.rows, r0 + p.rows_per_cta) - r0);
   const int nrw = warp < nr ? (nr - warp + kNW - 1) / kNW : 0;
-  const uint32_t omax = (uint32_t)p.rows * (uint32_t)p.chunks - 1u;
-  const uint32_t smax = (uint32_t)p.rows * (uint32_t)p.ngroups - 1u;
+  const uint32_t omax = (uint32_t)p.rows * (uint32_t)p.cstride - 1u;
+  const uint32_t smax = (uint32_t)p.rows * (uint32_t)p.gstride - 1u;
   // sz index step per chunk slot (32 chunks further along the row)
   const uint32_t sstep = (uint32_t)(32 * C::CPC) >> p.gshift;
 
@@ -261,10 +300,10 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
     const int nitems = nrw * cpl;
     // load cursor: item (row j, chunk slot i) -> element offsets
     const uint32_t row0 = (uint32_t)(r0 + warp);
-    uint32_t lo = row0 * (uint32_t)p.chunks + (uint32_t)(c0 + lane);
-    uint32_t ls = row0 * (uint32_t)p.ngroups + ((uint32_t)((c0 + lane) * C::CPC) >> p.gshift);
-    const uint32_t ojump = (uint32_t)(kNW * p.chunks) - 32u * (uint32_t)(cpl - 1);
-    const uint32_t sjump = (uint32_t)(kNW * p.ngroups) - sstep * (uint32_t)(cpl - 1);
+    uint32_t lo = row0 * (uint32_t)p.cstride + (uint32_t)(c0 + lane);
+    uint32_t ls = row0 * (uint32_t)p.gstride + ((uint32_t)((c0 + lane) * C::CPC) >> p.gshift);
+    const uint32_t ojump = (uint32_t)(kNW * p.cstride) - 32u * (uint32_t)(cpl - 1);
+    const uint32_t sjump = (uint32_t)(kNW * p.gstride) - sstep * (uint32_t)(cpl - 1);
     int li = 0;
     auto advance = [&]() {
       const bool wrap = ++li == cpl;
@@ -272,6 +311,23 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
       lo += wrap ? ojump : 32u;
       ls += wrap ? sjump : sstep;
     };
+
+#ifdef SGEMV_M1_L2PF
+    // ---- stage this CTA's rows of the packed weight into L2 with a few
+    // bulk prefetches (one contiguous range per array when K is one slice)
+    if (p.nslices == 1 && threadIdx.x < 3 && nr > 0) {
+      const size_t rb = (size_t)r0, re = (size_t)(r0 + nr);
+      if (threadIdx.x == 0)
+        prefetch_l2(p.vals + rb * p.cstride, (re - rb) * p.cstride * 16, p.vals,
+                    p.vals + (size_t)p.rows * p.cstride);
+      else if (threadIdx.x == 1)
+        prefetch_l2(p.idx + rb * p.cstride, (re - rb) * p.cstride * 8, p.idx,
+                    p.idx + (size_t)p.rows * p.cstride);
+      else
+        prefetch_l2(p.sz + rb * p.gstride, (re - rb) * p.gstride * 4, p.sz,
+                    p.sz + (size_t)p.rows * p.gstride);
+    }
+#endif
 
     Item<G2> it[kD];
 #pragma unroll
@@ -358,17 +414,19 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
       ci = 0;
       ++cj;
     };
-    // Items past the warp's last are computed on a fixed in-bounds element
-    // (one cached line, no extra DRAM traffic) and never written.
+    // Prefetches past the warp's last item read one fixed in-bounds element
+    // (a cached line, no extra DRAM traffic) and are never used.
     for (int k = 0; k < nitems; k += kD) {
 #pragma unroll
       for (int d = 0; d < kD; ++d) {
-        acc += chunk_dot<N, G2>(it[d].v, it[d].ix, it[d].sa, it[d].sb,
-                                lane_base + ci * kChunkSlotBytes);
-        const bool live = k + d + kD < nitems;
-        it[d].load(p, live ? lo : omax, live ? ls : smax, omax, smax);
-        advance();
-        if (ci == cpl - 1) finish_row(); else ++ci;
+        if (k + d < nitems) {
+          acc += chunk_dot<N, G2>(it[d].v, it[d].ix, it[d].sa, it[d].sb,
+                                  lane_base + ci * kChunkSlotBytes, magic);
+          const bool live = k + d + kD < nitems;
+          it[d].load(p, live ? lo : omax, live ? ls : smax, omax, smax);
+          advance();
+          if (ci == cpl - 1) finish_row(); else ++ci;
+        }
       }
     }
   }
@@ -394,13 +452,17 @@ cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   using C = M1Cfg<N>;
   const int chunks = (int)L.chunks;
   // 32-bit element offsets inside the kernel
-  if ((int64_t)L.rows * L.chunks >= (1ll << 31) || (int64_t)L.rows * L.ngroups >= (1ll << 31))
+  if ((int64_t)L.rows * L.cstride >= (1ll << 31) || (int64_t)L.rows * L.gstride >= (1ll << 31))
     return cudaErrorNotSupported;
   const int nslices = (chunks + 32 * C::MAX_CPL - 1) / (32 * C::MAX_CPL);
   const int cpl = (chunks + 32 * nslices - 1) / (32 * nslices);
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNotSupported;
-  int rows_per_cta = (L.rows + sms - 1) / sms;
+  const size_t smem_body = kTabAlign + (size_t)cpl * (C::TAB_PER_CPL + C::X_PER_CPL);
+  // CTAs per SM: as many as the shared memory allows, up to the launch bound
+  int per_sm = SGEMV_M1_GRIDB;
+  while (per_sm > 1 && smem_body * per_sm > (size_t)kSmemPerSm) --per_sm;
+  int rows_per_cta = (L.rows + sms * per_sm - 1) / (sms * per_sm);
   if (nslices > 1 && rows_per_cta > 1024) rows_per_cta = 1024;
   const int grid = (L.rows + rows_per_cta - 1) / rows_per_cta;
 
@@ -412,7 +474,8 @@ cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   p.y = a.y;
   p.rows = L.rows;
   p.cols = L.cols;
-  p.ngroups = (int)L.ngroups;
+  p.gstride = (int)L.gstride;
+  p.cstride = (int)L.cstride;
   p.gshift = L.group == 64 ? 6 : (L.group == 128 ? 7 : 8);
   p.chunks = chunks;
   p.rows_per_cta = rows_per_cta;
@@ -420,8 +483,7 @@ cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   p.slice_chunks = 32 * cpl;
   p.nslices = nslices;
 
-  const size_t smem = kTabAlign + (size_t)cpl * (C::TAB_PER_CPL + C::X_PER_CPL) +
-                      (nslices > 1 ? (size_t)rows_per_cta * 4 : 0);
+  const size_t smem = smem_body + (nslices > 1 ? (size_t)rows_per_cta * 4 : 0);
   if (smem > (size_t)kSmemLimit) return cudaErrorNotSupported;
   static bool attr_set[64] = {false};
   int dev = 0;
