@@ -84,6 +84,8 @@ int dev_err_to_status(int word) {
       return fail(SGEMV_ERR_RANGE, "a group's scale does not fit binary16");
     case sgemv::kDevErrBadIndex:
       return fail(SGEMV_ERR_ARG, "2:4 positions must ascend strictly within a quad");
+    case sgemv::kDevErrTimeout:
+      return fail(SGEMV_ERR_TIMEOUT, "a kernel's bounded wait for its weight copies gave up");
     default:
       return fail(SGEMV_ERR_CUDA, "device error word %d", word);
   }
@@ -311,6 +313,7 @@ static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s)
   a.x = static_cast<const __half*>(x);
   a.y = static_cast<__half*>(y);
   a.m = m;
+  a.err = h->d_err;
   if (m == 0 || L.rows == 0) return SGEMV_OK;
   // m = 1: the CUDA-core decode kernel; 2:4 with m >= 2: the sparse tensor
   // core kernel; anything else: the general kernel

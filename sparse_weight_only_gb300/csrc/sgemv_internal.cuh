@@ -79,6 +79,7 @@ namespace sgemv {
 constexpr int kDevErrNonfinite = 1;
 constexpr int kDevErrRange = 2;
 constexpr int kDevErrBadIndex = 3;
+constexpr int kDevErrTimeout = 4;
 
 // ---- format kernels (sgemv_format.cu) ----
 cudaError_t launch_pack(const Layout& L, const float* w, uint4* vals, uint2* idx,
@@ -100,6 +101,7 @@ struct RunArgs {
   const __half* x;
   __half* y;
   int m;
+  int* err;   // the handle's device error word
 };
 cudaError_t launch_generic(const Layout& L, const RunArgs& a, cudaStream_t s);
 // Each returns cudaErrorNotSupported when it does not cover the case.

@@ -5,9 +5,17 @@
 // fp32 accumulation, one rounding to binary16 per output.
 //
 // The work is bound by HBM bandwidth on the packed weight (0.81 bytes per
-// kept weight), so the kernel is built around issuing few instructions per
-// weight:
+// kept weight), so the kernel keeps many bytes in flight and issues few
+// instructions per weight:
 //
+//  * Weights stream through a per-warp ring of shared-memory stages filled
+//    by asynchronous copies (cp.async): each lane copies its 16 bytes of
+//    nibbles, 8 bytes of codes and its scale/zero word for the item two
+//    chunks ahead into a region only it reads, so no registers hold data in
+//    flight and no cross-lane synchronisation is needed.  The first stages
+//    are issued before the programmatic-dependent-launch wait, overlapping
+//    the previous kernel.  (Per-warp bulk TMA copies of the same stages were
+//    measured slower: the items are 128-512 B, too small for the TMA unit.)
 //  * Pair tables of x in shared memory.  A "pair unit" is two kept weights
 //    whose columns are fixed by one 4-bit code (2:4: the quad's two
 //    positions, 6 codes; 1:4: two adjacent quads' positions, 16 codes).  For
@@ -17,41 +25,28 @@
 //    128-byte line), so the data-dependent lookups never conflict.
 //  * INT4 decode by the exponent trick: OR-ing a nibble shifted by p into
 //    the mantissa of 2^23 gives the float 2^23 + q 2^p; subtracting
-//    2^23 + z 2^p is exact and leaves (q - z) 2^p.  Five nibbles decode in
-//    place, three after one shift; the 2^p factors are removed once per
-//    chunk in the epilogue.
+//    2^23 + z 2^p is exact and leaves (q - z) 2^p.  Each byte of a word is a
+//    pair unit; bytes 0, 1 decode in place, bytes 2, 3 after one shift; the
+//    2^p factors are removed once per chunk.
 //  * Packed f32x2 arithmetic (sm_100+) for the subtract and the FMA.
-//  * Each lane streams 16-byte value chunks and 8-byte index chunks with
-//    non-allocating loads, kept 4 chunks ahead in a register ring, so about
-//    14 KB per warp-iteration per SM are in flight.
 //  * Large K is cut into slices that fit the table; row partial sums carry
 //    over slices in shared memory.
-//  * The weight loads of the first chunks are issued before the
-//    programmatic-dependent-launch wait, so they overlap the previous
-//    kernel's tail; x is read only after the wait.
 #include "sgemv_internal.cuh"
 
 namespace sgemv {
 namespace {
 
-#ifndef SGEMV_M1_NT
-#define SGEMV_M1_NT 512
+#ifndef SGEMV_M1_S
+#define SGEMV_M1_S 2
 #endif
-#ifndef SGEMV_M1_D
-#define SGEMV_M1_D 2
-#endif
-#ifndef SGEMV_M1_MINB
-#define SGEMV_M1_MINB 1
-#endif
-#ifndef SGEMV_M1_GRIDB
-#define SGEMV_M1_GRIDB SGEMV_M1_MINB
-#endif
-constexpr int kNT = SGEMV_M1_NT;   // threads per CTA (one CTA per SM)
+constexpr int kNT = 512;            // threads per CTA (one CTA per SM)
 constexpr int kNW = kNT / 32;
-constexpr int kD = SGEMV_M1_D;     // prefetch depth in chunks
+constexpr int kS = SGEMV_M1_S;      // ring stages per warp (2 measured best)
+constexpr int kStage = 1024;        // bytes per stage
+constexpr int kIdxOff = 512;        // codes after the 512 B of nibbles
+constexpr int kSzOff = 768;         // scale/zero words after the codes
 constexpr int kSmemLimit = 227 * 1024;
 constexpr uint32_t kTabAlign = 2048;
-constexpr int kSmemPerSm = 228 * 1024;
 
 template <int N>
 struct M1Cfg {
@@ -59,10 +54,9 @@ struct M1Cfg {
   static constexpr int CPC = N == 2 ? 64 : 128;      // dense columns per chunk
   static constexpr int UC = N == 2 ? 4 : 8;          // dense columns per unit
   static constexpr int XPAD = CPC + 2;               // staged x per chunk (halves)
-  // shared bytes per chunk-per-lane of slice
+  // shared bytes per chunk-per-lane of a K slice
   static constexpr int TAB_PER_CPL = 32 * kUnitsPerChunk * E * 8;
   static constexpr int X_PER_CPL = 32 * XPAD * 2;
-  static constexpr int MAX_CPL = N == 2 ? 7 : 3;
 };
 
 struct M1Params {
@@ -71,6 +65,7 @@ struct M1Params {
   const uint32_t* sz;
   const __half* x;
   __half* y;
+  int* err;
   int rows, cols;
   int gstride;       // scale/zero words per row in memory
   int gshift;        // log2(group)
@@ -82,43 +77,43 @@ struct M1Params {
   int cpl;
 };
 
-__device__ __forceinline__ uint4 ld_stream16(const uint4* p) {
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void* src) {
+  if (BYTES == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(BYTES)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "r"(a));
   return v;
 }
-
-__device__ __forceinline__ uint2 ld_stream8(const uint2* p) {
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
   uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-               : "=r"(v.x), "=r"(v.y)
-               : "l"(p));
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
-
-__device__ __forceinline__ uint32_t ld_nc4(const uint32_t* p) {
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
-}
-
-// Asks the TMA unit to stage [p, p + bytes) into L2 (a hint: no data
-// returns to the SM).  The range is shrunk to whole 16-byte units inside
-// [lo, hi), the bounds of the buffer it belongs to.
-__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes, const void* lo,
-                                            const void* hi) {
-  uintptr_t a = (uintptr_t)p, b = a + bytes;
-  a = (a + 15) & ~(uintptr_t)15;
-  if (a < (uintptr_t)lo) a = ((uintptr_t)lo + 15) & ~(uintptr_t)15;
-  if (b > (uintptr_t)hi) b = (uintptr_t)hi;
-  b &= ~(uintptr_t)15;
-  while (a < b) {
-    const uint32_t n = (uint32_t)min((uintptr_t)65536, b - a);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
-    a += n;
-  }
 }
 
 template <int OFF>
@@ -134,12 +129,6 @@ __device__ __forceinline__ void sts_pair(uint32_t addr, float a, float b) {
   asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(addr), "f"(a), "f"(b));
 }
 
-__device__ __forceinline__ void pdl_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;");
-}
 
 // Subtract constants for one (scale, zero) group: -(2^23 + z 2^p) for the
 // nibble classes p = (0, 4) and (8, 12).
@@ -244,28 +233,76 @@ __device__ __forceinline__ float chunk_dot(const uint4& v, const uint2& ix,
   }
 }
 
-// Loads of one item (the chunk a lane handles for one row).  Offsets are
-// 32-bit element indices, clamped to the last element so that the zero-
-// contribution items past a ragged slice or past the last row never read
-// out of bounds (their table entries are zero).
-template <bool G2>
-struct Item {
-  uint4 v;
-  uint2 ix;
-  uint32_t sa, sb;
-  __device__ __forceinline__ void load(const M1Params& p, uint32_t o, uint32_t so,
-                                       uint32_t omax, uint32_t smax) {
-    o = min(o, omax);
-    so = min(so, smax);
-    v = ld_stream16(p.vals + o);
-    ix = ld_stream8(p.idx + o);
-    sa = ld_nc4(p.sz + so);
-    if (G2) sb = ld_nc4(p.sz + min(so + 1, smax));
+// Local row (within the CTA's block of nr rows) of a warp's j-th row.  With
+// SGEMV_M1_CONSEC each warp takes a contiguous run of rows, so its copies
+// walk memory sequentially; otherwise rows interleave across warps.
+#ifdef SGEMV_M1_CONSEC
+__device__ __forceinline__ int warp_row(int warp, int j, int nr) {
+  return warp * ((nr + kNW - 1) / kNW) + j;
+}
+__device__ __forceinline__ int warp_nrows(int warp, int nr) {
+  const int q = (nr + kNW - 1) / kNW;
+  return max(0, min(q, nr - warp * q));
+}
+#else
+__device__ __forceinline__ int warp_row(int warp, int j, int) { return warp + kNW * j; }
+__device__ __forceinline__ int warp_nrows(int warp, int nr) {
+  return warp < nr ? (nr - warp + kNW - 1) / kNW : 0;
+}
+#endif
+
+// Position of a warp in its item sequence: K slice, row of the warp, chunk
+// slot.  Item k of a warp is the slot'th group of 32 chunks of its j'th row
+// in slice sl.
+struct Cursor {
+  int sl, j, i;
+  int c0, nch, cpl;
+  __device__ __forceinline__ void start(const M1Params& p, int s) {
+    sl = s;
+    j = 0;
+    i = 0;
+    c0 = s * p.slice_chunks;
+    nch = min(p.slice_chunks, p.chunks - c0);
+    cpl = (nch + 31) >> 5;
+  }
+  // false once past the last slice
+  __device__ __forceinline__ bool next(const M1Params& p, int nrw) {
+    if (++i < cpl) return true;
+    i = 0;
+    if (++j < nrw) return true;
+    if (sl + 1 >= p.nslices) {
+      ++sl;
+      return false;
+    }
+    start(p, sl + 1);
+    return true;
   }
 };
 
+// Copies this lane's part of item `c` into the stage with per-lane
+// asynchronous copies: its 16 bytes of nibbles, 8 bytes of codes and its
+// scale/zero word(s), each into a region of the stage only this lane reads.
+// Lanes past a ragged slice copy nothing (their results are discarded).
 template <int N, bool G2>
-__global__ void __launch_bounds__(kNT, SGEMV_M1_MINB) k_m1(M1Params p) {
+__device__ __forceinline__ void issue_item(const M1Params& p, const Cursor& c, int r0, int nr,
+                                           int warp, int lane, uint32_t stage) {
+  using C = M1Cfg<N>;
+  const int ch = c.c0 + 32 * c.i + lane;
+  if (ch < c.c0 + c.nch) {
+    const int row = r0 + warp_row(warp, c.j, nr);
+    const size_t rc = (size_t)row * p.cstride + ch;
+    cp_async<16>(stage + 16 * lane, p.vals + rc);
+    cp_async<8>(stage + kIdxOff + 8 * lane, p.idx + rc);
+    const uint32_t* sp = p.sz + (size_t)row * p.gstride + ((ch * C::CPC) >> p.gshift);
+    if (G2)
+      cp_async<8>(stage + kSzOff + 8 * lane, sp);
+    else
+      cp_async<4>(stage + kSzOff + 8 * lane, sp);
+  }
+}
+
+template <int N, bool G2>
+__global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   using C = M1Cfg<N>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
@@ -278,68 +315,48 @@ __global__ void __launch_bounds__(kNT, SGEMV_M1_MINB) k_m1(M1Params p) {
   const uint32_t pad = (kTabAlign - (raw_s & (kTabAlign - 1))) & (kTabAlign - 1);
   unsigned char* tab = smem + pad;
   const uint32_t smem_s = raw_s + pad;
+  const int xs_bytes = p.slice_chunks * C::XPAD * 2;
   __half* xs = reinterpret_cast<__half*>(tab + tab_bytes);
-  float* part = reinterpret_cast<float*>(tab + tab_bytes + p.slice_chunks * C::XPAD * 2);
+  float* part = reinterpret_cast<float*>(tab + tab_bytes + xs_bytes);
+  const int part_bytes = (p.nslices > 1 ? (p.rows_per_cta * 4 + 127) & ~127 : 0);
+  const uint32_t ring_s = smem_s + (uint32_t)(tab_bytes + xs_bytes + part_bytes);
+  const uint32_t my_ring = ring_s + (uint32_t)(warp * kS * kStage);
   const uint32_t lane_base = smem_s + (uint32_t)((lane >> 4) * S) * 128u + (lane & 15) * 8u;
   constexpr uint32_t kChunkSlotBytes = kUnitsPerChunk * C::E * 128;
-
   uint32_t magic = 0x4B000000u;  // exponent of 2^23, kept in a register
   asm volatile("" : "+r"(magic));
+
   const int r0 = blockIdx.x * p.rows_per_cta;
   const int nr = max(0, min(p.rows, r0 + p.rows_per_cta) - r0);
-  const int nrw = warp < nr ? (nr - warp + kNW - 1) / kNW : 0;
-  const uint32_t omax = (uint32_t)p.rows * (uint32_t)p.cstride - 1u;
-  const uint32_t smax = (uint32_t)p.rows * (uint32_t)p.gstride - 1u;
-  // sz index step per chunk slot (32 chunks further along the row)
-  const uint32_t sstep = (uint32_t)(32 * C::CPC) >> p.gshift;
+  const int nrw = warp_nrows(warp, nr);
 
+  // ---- the first kS items into the ring (weights only: no dependence on
+  // the previous kernel); one commit group per item, empty past the end
+  // The ring starts zeroed: a lane past a ragged slice reads a stage it did
+  // not fill, and must find codes in range there (its table slots are zero).
+  for (int b = 16 * lane; b < kS * kStage; b += 16 * 32)
+    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(my_ring + b), "r"(0u) : "memory");
+  __syncwarp();
+  Cursor prod;
+  prod.start(p, 0);
+  bool more = nrw > 0;
+  for (int st = 0; st < kS; ++st) {
+    if (more) {
+      issue_item<N, G2>(p, prod, r0, nr, warp, lane, my_ring + st * kStage);
+      more = prod.next(p, nrw);
+    }
+    cp_commit();
+  }
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  int consumed = 0;
   for (int sl = 0; sl < p.nslices; ++sl) {
     const int c0 = sl * p.slice_chunks;
     const int nch = min(p.slice_chunks, p.chunks - c0);
     const int cpl = (nch + 31) >> 5;
     const int nitems = nrw * cpl;
-    // load cursor: item (row j, chunk slot i) -> element offsets
-    const uint32_t row0 = (uint32_t)(r0 + warp);
-    uint32_t lo = row0 * (uint32_t)p.cstride + (uint32_t)(c0 + lane);
-    uint32_t ls = row0 * (uint32_t)p.gstride + ((uint32_t)((c0 + lane) * C::CPC) >> p.gshift);
-    const uint32_t ojump = (uint32_t)(kNW * p.cstride) - 32u * (uint32_t)(cpl - 1);
-    const uint32_t sjump = (uint32_t)(kNW * p.gstride) - sstep * (uint32_t)(cpl - 1);
-    int li = 0;
-    auto advance = [&]() {
-      const bool wrap = ++li == cpl;
-      li = wrap ? 0 : li;
-      lo += wrap ? ojump : 32u;
-      ls += wrap ? sjump : sstep;
-    };
-
-#ifdef SGEMV_M1_L2PF
-    // ---- stage this CTA's rows of the packed weight into L2 with a few
-    // bulk prefetches (one contiguous range per array when K is one slice)
-    if (p.nslices == 1 && threadIdx.x < 3 && nr > 0) {
-      const size_t rb = (size_t)r0, re = (size_t)(r0 + nr);
-      if (threadIdx.x == 0)
-        prefetch_l2(p.vals + rb * p.cstride, (re - rb) * p.cstride * 16, p.vals,
-                    p.vals + (size_t)p.rows * p.cstride);
-      else if (threadIdx.x == 1)
-        prefetch_l2(p.idx + rb * p.cstride, (re - rb) * p.cstride * 8, p.idx,
-                    p.idx + (size_t)p.rows * p.cstride);
-      else
-        prefetch_l2(p.sz + rb * p.gstride, (re - rb) * p.gstride * 4, p.sz,
-                    p.sz + (size_t)p.rows * p.gstride);
-    }
-#endif
-
-    Item<G2> it[kD];
-#pragma unroll
-    for (int d = 0; d < kD; ++d) {
-      if (d < nitems) it[d].load(p, lo, ls, omax, smax);
-      advance();
-    }
-
-    if (sl == 0) {
-      pdl_wait();
-      pdl_launch_dependents();
-    }
     __syncthreads();  // the previous slice's table is no longer read
 
     // ---- stage x of the slice (binary16, zero past cols), padded per chunk
@@ -391,45 +408,56 @@ __global__ void __launch_bounds__(kNT, SGEMV_M1_MINB) k_m1(M1Params p) {
     }
     __syncthreads();
 
-    // ---- stream the rows: compute item k from ring slot k % kD, then load
-    // item k + kD into that slot
+    // ---- stream the rows of this slice
     int ci = 0, cj = 0;  // (chunk slot, row) of the item being computed
     float acc = 0.0f;
-    auto finish_row = [&]() {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (lane == 0 && cj < nrw) {
-        const int rl = warp + kNW * cj;
-        if (p.nslices == 1) {
-          p.y[r0 + rl] = __float2half_rn(acc);
-        } else {
-          const float t = (sl ? part[rl] : 0.0f) + acc;
-          if (sl == p.nslices - 1)
-            p.y[r0 + rl] = __float2half_rn(t);
-          else
-            part[rl] = t;
-        }
+    for (int k = 0; k < nitems; ++k, ++consumed) {
+      const int st = consumed % kS;
+      const uint32_t stage = my_ring + st * kStage;
+      cp_wait<kS - 1>();   // this lane's copies of item `consumed` landed
+      const bool valid = lane + 32 * ci < nch;
+      const uint4 v = lds128(stage + 16 * lane);
+      const uint2 ix = lds64(stage + kIdxOff + 8 * lane);
+      uint32_t sa, sb = 0;
+      if (G2) {
+        const uint2 s2 = lds64(stage + kSzOff + 8 * lane);
+        sa = s2.x;
+        sb = s2.y;
+      } else {
+        sa = lds32(stage + kSzOff + 8 * lane);
       }
-      acc = 0.0f;
-      ci = 0;
-      ++cj;
-    };
-    // Prefetches past the warp's last item read one fixed in-bounds element
-    // (a cached line, no extra DRAM traffic) and are never used.
-    for (int k = 0; k < nitems; k += kD) {
+      if (!valid) { sa = 0u; sb = 0u; }   // ragged slice: zero contribution
+      // refill the stage this lane just read with item consumed + kS
+      if (more) {
+        issue_item<N, G2>(p, prod, r0, nr, warp, lane, stage);
+        more = prod.next(p, nrw);
+      }
+      cp_commit();
+      acc += chunk_dot<N, G2>(v, ix, sa, sb, lane_base + ci * kChunkSlotBytes, magic);
+      if (ci == cpl - 1) {
 #pragma unroll
-      for (int d = 0; d < kD; ++d) {
-        if (k + d < nitems) {
-          acc += chunk_dot<N, G2>(it[d].v, it[d].ix, it[d].sa, it[d].sb,
-                                  lane_base + ci * kChunkSlotBytes, magic);
-          const bool live = k + d + kD < nitems;
-          it[d].load(p, live ? lo : omax, live ? ls : smax, omax, smax);
-          advance();
-          if (ci == cpl - 1) finish_row(); else ++ci;
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+          const int rl = warp_row(warp, cj, nr);
+          if (p.nslices == 1) {
+            p.y[r0 + rl] = __float2half_rn(acc);
+          } else {
+            const float t = (sl ? part[rl] : 0.0f) + acc;
+            if (sl == p.nslices - 1)
+              p.y[r0 + rl] = __float2half_rn(t);
+            else
+              part[rl] = t;
+          }
         }
+        acc = 0.0f;
+        ci = 0;
+        ++cj;
+      } else {
+        ++ci;
       }
     }
   }
+  cp_wait<0>();  // no copy outstanding when the CTA retires
 }
 
 int g_num_sms[64] = {0};
@@ -451,18 +479,18 @@ template <int N, bool G2>
 cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   using C = M1Cfg<N>;
   const int chunks = (int)L.chunks;
-  // 32-bit element offsets inside the kernel
   if ((int64_t)L.rows * L.cstride >= (1ll << 31) || (int64_t)L.rows * L.gstride >= (1ll << 31))
     return cudaErrorNotSupported;
-  const int nslices = (chunks + 32 * C::MAX_CPL - 1) / (32 * C::MAX_CPL);
-  const int cpl = (chunks + 32 * nslices - 1) / (32 * nslices);
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNotSupported;
-  const size_t smem_body = kTabAlign + (size_t)cpl * (C::TAB_PER_CPL + C::X_PER_CPL);
-  // CTAs per SM: as many as the shared memory allows, up to the launch bound
-  int per_sm = SGEMV_M1_GRIDB;
-  while (per_sm > 1 && smem_body * per_sm > (size_t)kSmemPerSm) --per_sm;
-  int rows_per_cta = (L.rows + sms * per_sm - 1) / (sms * per_sm);
+  const size_t ring = (size_t)kNW * kS * kStage;
+  const size_t part_max = 4096;   // rows_per_cta <= 1024 when K is sliced
+  const size_t room = kSmemLimit - kTabAlign - ring - part_max;
+  const int max_cpl = (int)(room / (C::TAB_PER_CPL + C::X_PER_CPL));
+  if (max_cpl < 1) return cudaErrorNotSupported;
+  const int nslices = (chunks + 32 * max_cpl - 1) / (32 * max_cpl);
+  const int cpl = (chunks + 32 * nslices - 1) / (32 * nslices);
+  int rows_per_cta = (L.rows + sms - 1) / sms;
   if (nslices > 1 && rows_per_cta > 1024) rows_per_cta = 1024;
   const int grid = (L.rows + rows_per_cta - 1) / rows_per_cta;
 
@@ -472,6 +500,7 @@ cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   p.sz = a.sz;
   p.x = a.x;
   p.y = a.y;
+  p.err = a.err;
   p.rows = L.rows;
   p.cols = L.cols;
   p.gstride = (int)L.gstride;
@@ -483,7 +512,8 @@ cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   p.slice_chunks = 32 * cpl;
   p.nslices = nslices;
 
-  const size_t smem = smem_body + (nslices > 1 ? (size_t)rows_per_cta * 4 : 0);
+  const size_t part_bytes = nslices > 1 ? ((size_t)rows_per_cta * 4 + 127) & ~(size_t)127 : 0;
+  const size_t smem = kTabAlign + (size_t)cpl * (C::TAB_PER_CPL + C::X_PER_CPL) + part_bytes + ring;
   if (smem > (size_t)kSmemLimit) return cudaErrorNotSupported;
   static bool attr_set[64] = {false};
   int dev = 0;
