@@ -161,6 +161,10 @@ class ClockSampler:
 # the workload
 # ---------------------------------------------------------------------------
 
+# matrices of the layer that share one activation x
+GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+
+
 def workload(seed: int = 0):
     return synth.config3(seed)
 
@@ -303,21 +307,39 @@ def run_ours(args, rank, world, local):
             cp.append(h)
         sets.append(cp)
 
-    xs = [torch.from_numpy(gv.x(m)).to(dev) for gv in gvs]
+    # x is shared where a decoder layer shares it: q, k, v read one x and
+    # gate, up read one x; o and down have their own
+    pos = {g.name: i for i, g in enumerate(gvs)}
+    groups = [[pos[n] for n in grp] for grp in GROUPS]
+    xs = [None] * len(gvs)
+    for grp in groups:
+        x0 = torch.from_numpy(gvs[grp[0]].x(m)).to(dev)
+        for i in grp:
+            xs[i] = x0
     ys = [torch.empty((m, gv.rows), dtype=torch.float16, device=dev) for gv in gvs]
     stream = torch.cuda.Stream(device=dev)
     sptr = stream.cuda_stream
+    grouped = not args.ungrouped
 
-    def launch_step(k):
-        for h, x, y in zip(sets[k % copies], xs, ys):
-            h.run(x, y, sptr)
+    def launch_step(k, grouped=grouped):
+        st = sets[k % copies]
+        if grouped:
+            for grp in groups:
+                if len(grp) == 1:
+                    st[grp[0]].run(xs[grp[0]], ys[grp[0]], sptr)
+                else:
+                    swo.run_group([st[i] for i in grp], xs[grp[0]],
+                                  [ys[i] for i in grp], sptr)
+        else:
+            for h, x, y in zip(st, xs, ys):
+                h.run(x, y, sptr)
 
-    def capture(nsteps, first):
+    def capture(nsteps, first, grouped=grouped):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
                 for k in range(nsteps):
-                    launch_step(first + k)
+                    launch_step(first + k, grouped)
         return g
 
     # graphs: a block of `copies` steps (each copy once) and a remainder
@@ -325,13 +347,14 @@ def run_ours(args, rank, world, local):
     with torch.cuda.stream(stream):
         for k in range(2):
             launch_step(k)            # eager warm-up before capture
+            launch_step(k, not grouped)
     torch.cuda.synchronize()
     g_block = capture(block, 0)
 
-    def replay(nsteps, rem_graphs):
+    def replay(nsteps, rem_graphs, gb=None):
         q, r = divmod(nsteps, block)
         for _ in range(q):
-            g_block.replay()
+            (gb or g_block).replay()
         if r:
             rem_graphs[r].replay()
 
@@ -361,7 +384,32 @@ def run_ours(args, rank, world, local):
     total_bytes = sum_over_ranks(sb * args.steps, world, dev)
     value = total_bytes / t_max / 1e9
     ms_step = 1e3 * t_max / args.steps
-    launches = len(gvs) * args.steps
+    if grouped:
+        per_step = sum(len({gvs[i].n_keep for i in grp}) for grp in groups)
+    else:
+        per_step = len(gvs)
+    launches = per_step * args.steps
+
+    # the other launch mode, same steps, for comparison
+    g_other = capture(block, 0, not grouped)
+    rem_o = {}
+    if args.steps % block:
+        rem_o[args.steps % block] = capture(args.steps % block, 0, not grouped)
+    with torch.cuda.stream(stream):
+        g_other.replay()              # warm-up: one block of steps
+    torch.cuda.synchronize()
+    o0 = torch.cuda.Event(enable_timing=True)
+    o1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        o0.record(stream)
+        replay(args.steps, rem_o, g_other)
+        o1.record(stream)
+    torch.cuda.synchronize()
+    t_other = o0.elapsed_time(o1) / 1e3
+    other = {"mode": "per-matrix calls" if grouped else "grouped calls",
+             "ms_per_step": 1e3 * t_other / args.steps,
+             "gbs": sb * args.steps / t_other / 1e9}
+    del g_other, rem_o
 
     # correctness of what was timed: all copies produce identical y
     y_check = [y.clone() for y in ys]
@@ -508,6 +556,9 @@ def run_ours(args, rank, world, local):
         "pack_seconds": round(t_pack, 3),
         "batch_m": batch,
         "copies_identical_y": same,
+        "launch_mode": ("grouped calls: run_group(q,k,v), run(o), run_group(gate,up), "
+                        "run(down)" if grouped else "per-matrix calls"),
+        "other_launch_mode": other,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -585,6 +636,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ungrouped", action="store_true",
+                    help="time one call per matrix instead of the grouped calls")
     ap.add_argument("--no-batch", action="store_true",
                     help="skip the small-M (config 4) sweep")
     args = ap.parse_args(argv)

@@ -135,6 +135,26 @@ int sgemv_run(sgemv_t h, const void* x_dev, void* y_dev, int m, void* stream);
 int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
                    void* stream);
 
+/*
+ * Several products that share one activation x -- e.g. the q, k and v
+ * projections of a decoder layer, or its gate and up projections -- as
+ * y_i = W_hat_i . x for i < count.  This is the grouped run of the
+ * layer's decode step (the paper's kernel serves every linear layer of the
+ * decode, section 1 contribution 2): with m = 1 the matrices of each N go
+ * into one launch that stages x and its lookup tables once per CTA for all
+ * of them (at most 8 per launch, more launches beyond that); with m > 1 each
+ * matrix runs as in sgemv_run.
+ *   handles : count packed handles on one device, all with the same cols;
+ *             n_keep and group may differ;
+ *   x_dev   : m x cols binary16, 16-byte aligned, shared by all;
+ *   y_devs  : count device pointers, y_devs[i] is m x rows_i binary16,
+ *             2-byte aligned, none overlapping x_dev;
+ *   m       : 0 <= m <= every handle's max_m.
+ * Asynchronous on `stream`, like sgemv_run; count = 0 is a no-op.
+ */
+int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
+                    void* const* y_devs, int m, void* stream);
+
 /* Synchronise the device, then return and clear the handle's device error
  * word (SGEMV_OK if no kernel reported an error since the last call). */
 int sgemv_status(sgemv_t h);

@@ -38,6 +38,7 @@ SIGNATURES = {
     "sgemv_export": (_I, [_P, _P, _P, _P, _P]),
     "sgemv_run": (_I, [_P, _P, _P, _I, _P]),
     "sgemv_run_host": (_I, [_P, _P, _P, _I, _P]),
+    "sgemv_run_group": (_I, [_P, _I, _P, _P, _I, _P]),
     "sgemv_status": (_I, [_P]),
     "sgemv_sizes": (_I, [_P, _PSZ, _PSZ, _PSZ, _PSZ]),
     "sgemv_packed_bytes": (_SZ, [_P]),
@@ -206,3 +207,17 @@ class SparseGemv:
 
     def status(self) -> int:
         return int(load().sgemv_status(self._h))
+
+
+def run_group(mats, x, ys, stream=None) -> None:
+    """y_i = W_hat_i . x for matrices that share x (one launch per N at
+    m = 1).  mats: SparseGemv list; x: (m, cols) fp16 CUDA tensor; ys: list
+    of (m, rows_i) fp16 CUDA tensors."""
+    n = len(mats)
+    if len(ys) != n:
+        raise ValueError("one output per matrix")
+    hs = (ctypes.c_void_p * max(n, 1))(*[h.handle for h in mats])
+    yp = (ctypes.c_void_p * max(n, 1))(*[y.data_ptr() for y in ys])
+    m = x.shape[0] if x.dim() == 2 else 1
+    _check(load().sgemv_run_group(hs, n, x.data_ptr(), yp, m, _stream_ptr(stream)),
+           "sgemv_run_group")

@@ -374,6 +374,81 @@ int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
   return SGEMV_OK;
 }
 
+int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
+                    void* const* y_devs, int m, void* stream) {
+  if (count < 0) return fail(SGEMV_ERR_ARG, "count=%d is negative", count);
+  if (count == 0) return SGEMV_OK;
+  if (!handles || !y_devs) return fail(SGEMV_ERR_ARG, "handles or y_devs is NULL");
+  for (int i = 0; i < count; ++i) {
+    if (int rc = run_args_ok(handles[i], x_dev, y_devs[i], m)) return rc;
+    if (handles[i]->L.cols != handles[0]->L.cols)
+      return fail(SGEMV_ERR_ARG, "handle %d has cols=%d, handle 0 has cols=%d", i,
+                  handles[i]->L.cols, handles[0]->L.cols);
+    if (handles[i]->device != handles[0]->device)
+      return fail(SGEMV_ERR_ARG, "handles are on different devices");
+    if (y_devs[i] && ((uintptr_t)y_devs[i] & 1u))
+      return fail(SGEMV_ERR_ARG, "y_devs[%d] must be 2-byte aligned", i);
+    if (m > 0 && x_dev && y_devs[i]) {
+      const char* xb = static_cast<const char*>(x_dev);
+      const char* yb = static_cast<const char*>(y_devs[i]);
+      const size_t xn = (size_t)m * handles[i]->L.cols * 2;
+      const size_t yn = (size_t)m * handles[i]->L.rows * 2;
+      if (xn && yn && xb < yb + yn && yb < xb + xn)
+        return fail(SGEMV_ERR_ARG, "x and y_devs[%d] overlap", i);
+    }
+  }
+  if (x_dev && ((uintptr_t)x_dev & 15u))
+    return fail(SGEMV_ERR_ARG, "x_dev must be 16-byte aligned");
+  DeviceGuard g(handles[0]->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (m == 0 || handles[0]->L.cols == 0) {
+    for (int i = 0; i < count; ++i)
+      if (int rc = run_checked(handles[i], x_dev, y_devs[i], m, s)) return rc;
+    return SGEMV_OK;
+  }
+  if (m != 1) {
+    for (int i = 0; i < count; ++i)
+      if (int rc = run_checked(handles[i], x_dev, y_devs[i], m, s)) return rc;
+    return SGEMV_OK;
+  }
+  // m = 1: one launch per N for up to max_group() matrices
+  const int cap = sgemv::max_group();
+  for (int n = 1; n <= 2; ++n) {
+    sgemv::Layout Ls[8];
+    sgemv::RunArgs as[8];
+    int k = 0;
+    for (int i = 0; i <= count; ++i) {
+      const bool take = i < count && handles[i]->L.n_keep == n && handles[i]->L.rows > 0;
+      if (take) {
+        sgemv_t h = handles[i];
+        Ls[k] = h->L;
+        as[k].vals = h->d_vals;
+        as[k].idx = h->d_idx;
+        as[k].sz = h->d_sz;
+        as[k].x = static_cast<const __half*>(x_dev);
+        as[k].y = static_cast<__half*>(y_devs[i]);
+        as[k].m = 1;
+        as[k].err = h->d_err;
+        ++k;
+      }
+      if (k > 0 && (k == cap || i == count)) {
+        cudaError_t e = sgemv::launch_m1_group(Ls, as, k, s);
+        if (e == cudaErrorNotSupported) {
+          (void)cudaGetLastError();
+          for (int q = 0; q < k; ++q) {
+            e = sgemv::launch_generic(Ls[q], as[q], s);
+            if (e != cudaSuccess) break;
+          }
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "grouped SparseGemv launch");
+        k = 0;
+      }
+    }
+  }
+  return SGEMV_OK;
+}
+
 int sgemv_status(sgemv_t h) {
   if (int rc = check_handle(h)) return rc;
   DeviceGuard g(h->device);

@@ -107,5 +107,8 @@ cudaError_t launch_generic(const Layout& L, const RunArgs& a, cudaStream_t s);
 // Each returns cudaErrorNotSupported when it does not cover the case.
 cudaError_t launch_m1(const Layout& L, const RunArgs& a, cudaStream_t s);
 cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s);
+// m = 1 over several matrices sharing x, cols and N in one launch.
+cudaError_t launch_m1_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s);
+int max_group();
 
 }  // namespace sgemv

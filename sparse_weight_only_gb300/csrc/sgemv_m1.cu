@@ -31,6 +31,8 @@
 //  * Packed f32x2 arithmetic (sm_100+) for the subtract and the FMA.
 //  * Large K is cut into slices that fit the table; row partial sums carry
 //    over slices in shared memory.
+#include <string.h>
+
 #include "sgemv_internal.cuh"
 
 namespace sgemv {
@@ -59,16 +61,26 @@ struct M1Cfg {
   static constexpr int X_PER_CPL = 32 * XPAD * 2;
 };
 
-struct M1Params {
+// One packed matrix of a launch.  A launch covers up to kMaxSeg matrices
+// that share x (and N): their rows are concatenated into one row space.
+constexpr int kMaxSeg = 8;
+struct M1Seg {
   const uint4* vals;
   const uint2* idx;
   const uint32_t* sz;
-  const __half* x;
   __half* y;
-  int* err;
-  int rows, cols;
+  int row_begin;     // first row of this matrix in the launch's row space
   int gstride;       // scale/zero words per row in memory
   int gshift;        // log2(group)
+  int g64;           // 1:4 with 64-column groups: two groups per chunk
+};
+
+struct M1Params {
+  M1Seg seg[kMaxSeg];
+  int nseg;
+  const __half* x;
+  int* err;
+  int rows, cols;    // rows of all matrices together
   int chunks;        // chunks holding a row's kept weights
   int cstride;       // chunks per row in memory
   int rows_per_cta;
@@ -76,6 +88,15 @@ struct M1Params {
   int nslices;
   int cpl;
 };
+
+// Matrix holding row `row` of the launch's row space (warp-uniform).
+__device__ __forceinline__ int find_seg(const M1Params& p, int row) {
+  int s = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxSeg; ++i)
+    if (i < p.nseg && row >= p.seg[i].row_begin) s = i;
+  return s;
+}
 
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -254,27 +275,51 @@ __device__ __forceinline__ int warp_nrows(int warp, int nr) {
 // Position of a warp in its item sequence: K slice, row of the warp, chunk
 // slot.  Item k of a warp is the slot'th group of 32 chunks of its j'th row
 // in slice sl.
+// MODE of a launch: kOne = one matrix, groups of 64 columns not split
+// across chunks; kOneG64 = one 1:4 matrix with 64-column groups (two groups
+// per chunk); kMany = several matrices, the split decided per row.
+constexpr int kOne = 0, kOneG64 = 1, kMany = 2;
+
+template <int MODE>
 struct Cursor {
   int sl, j, i;
   int c0, nch, cpl;
-  __device__ __forceinline__ void start(const M1Params& p, int s) {
+  // the row of item (sl, j): its matrix's rows of nibbles, codes, scales
+  const uint4* vrow;
+  const uint2* irow;
+  const uint32_t* srow;
+  int gshift, g64;
+  __device__ __forceinline__ void set_row(const M1Params& p, int row) {
+    const M1Seg& sg = p.seg[MODE == kMany ? find_seg(p, row) : 0];
+    const int lr = row - sg.row_begin;
+    vrow = sg.vals + (size_t)lr * p.cstride;
+    irow = sg.idx + (size_t)lr * p.cstride;
+    srow = sg.sz + (size_t)lr * sg.gstride;
+    gshift = sg.gshift;
+    g64 = MODE == kMany ? sg.g64 : (MODE == kOneG64);
+  }
+  __device__ __forceinline__ void start(const M1Params& p, int s, int r0, int warp, int nr) {
     sl = s;
     j = 0;
     i = 0;
     c0 = s * p.slice_chunks;
     nch = min(p.slice_chunks, p.chunks - c0);
     cpl = (nch + 31) >> 5;
+    if (warp_nrows(warp, nr) > 0) set_row(p, r0 + warp_row(warp, 0, nr));
   }
   // false once past the last slice
-  __device__ __forceinline__ bool next(const M1Params& p, int nrw) {
+  __device__ __forceinline__ bool next(const M1Params& p, int nrw, int r0, int warp, int nr) {
     if (++i < cpl) return true;
     i = 0;
-    if (++j < nrw) return true;
+    if (++j < nrw) {
+      set_row(p, r0 + warp_row(warp, j, nr));
+      return true;
+    }
     if (sl + 1 >= p.nslices) {
       ++sl;
       return false;
     }
-    start(p, sl + 1);
+    start(p, sl + 1, r0, warp, nr);
     return true;
   }
 };
@@ -283,25 +328,22 @@ struct Cursor {
 // asynchronous copies: its 16 bytes of nibbles, 8 bytes of codes and its
 // scale/zero word(s), each into a region of the stage only this lane reads.
 // Lanes past a ragged slice copy nothing (their results are discarded).
-template <int N, bool G2>
-__device__ __forceinline__ void issue_item(const M1Params& p, const Cursor& c, int r0, int nr,
-                                           int warp, int lane, uint32_t stage) {
+template <int N, int MODE>
+__device__ __forceinline__ void issue_item(const Cursor<MODE>& c, int lane, uint32_t stage) {
   using C = M1Cfg<N>;
   const int ch = c.c0 + 32 * c.i + lane;
   if (ch < c.c0 + c.nch) {
-    const int row = r0 + warp_row(warp, c.j, nr);
-    const size_t rc = (size_t)row * p.cstride + ch;
-    cp_async<16>(stage + 16 * lane, p.vals + rc);
-    cp_async<8>(stage + kIdxOff + 8 * lane, p.idx + rc);
-    const uint32_t* sp = p.sz + (size_t)row * p.gstride + ((ch * C::CPC) >> p.gshift);
-    if (G2)
+    cp_async<16>(stage + 16 * lane, c.vrow + ch);
+    cp_async<8>(stage + kIdxOff + 8 * lane, c.irow + ch);
+    const uint32_t* sp = c.srow + ((ch * C::CPC) >> c.gshift);
+    if (N == 1 && (MODE == kOneG64 || (MODE == kMany && c.g64)))
       cp_async<8>(stage + kSzOff + 8 * lane, sp);
     else
       cp_async<4>(stage + kSzOff + 8 * lane, sp);
   }
 }
 
-template <int N, bool G2>
+template <int N, int MODE>
 __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   using C = M1Cfg<N>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -337,13 +379,13 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   for (int b = 16 * lane; b < kS * kStage; b += 16 * 32)
     asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(my_ring + b), "r"(0u) : "memory");
   __syncwarp();
-  Cursor prod;
-  prod.start(p, 0);
+  Cursor<MODE> prod;
+  prod.start(p, 0, r0, warp, nr);
   bool more = nrw > 0;
   for (int st = 0; st < kS; ++st) {
     if (more) {
-      issue_item<N, G2>(p, prod, r0, nr, warp, lane, my_ring + st * kStage);
-      more = prod.next(p, nrw);
+      issue_item<N, MODE>(prod, lane, my_ring + st * kStage);
+      more = prod.next(p, nrw, r0, warp, nr);
     }
     cp_commit();
   }
@@ -411,40 +453,50 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
     // ---- stream the rows of this slice
     int ci = 0, cj = 0;  // (chunk slot, row) of the item being computed
     float acc = 0.0f;
+    __half* yrow = nullptr;  // output element of the current row
+    bool g64 = false;
     for (int k = 0; k < nitems; ++k, ++consumed) {
+      if (ci == 0) {
+        const int row = r0 + warp_row(warp, cj, nr);
+        const M1Seg& sg = p.seg[MODE == kMany ? find_seg(p, row) : 0];
+        yrow = sg.y + (row - sg.row_begin);
+        g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
+      }
       const int st = consumed % kS;
       const uint32_t stage = my_ring + st * kStage;
       cp_wait<kS - 1>();   // this lane's copies of item `consumed` landed
       const bool valid = lane + 32 * ci < nch;
       const uint4 v = lds128(stage + 16 * lane);
       const uint2 ix = lds64(stage + kIdxOff + 8 * lane);
-      uint32_t sa, sb = 0;
-      if (G2) {
-        const uint2 s2 = lds64(stage + kSzOff + 8 * lane);
-        sa = s2.x;
-        sb = s2.y;
-      } else {
-        sa = lds32(stage + kSzOff + 8 * lane);
-      }
-      if (!valid) { sa = 0u; sb = 0u; }   // ragged slice: zero contribution
+      const uint2 s2 = lds64(stage + kSzOff + 8 * lane);
+      const uint32_t sa = valid ? s2.x : 0u;   // ragged slice: zero contribution
+      const uint32_t sb = valid ? s2.y : 0u;
       // refill the stage this lane just read with item consumed + kS
       if (more) {
-        issue_item<N, G2>(p, prod, r0, nr, warp, lane, stage);
-        more = prod.next(p, nrw);
+        issue_item<N, MODE>(prod, lane, stage);
+        more = prod.next(p, nrw, r0, warp, nr);
       }
       cp_commit();
-      acc += chunk_dot<N, G2>(v, ix, sa, sb, lane_base + ci * kChunkSlotBytes, magic);
+      const uint32_t tb = lane_base + ci * kChunkSlotBytes;
+      if constexpr (N == 1 && MODE == kMany) {
+        if (g64)
+          acc += chunk_dot<N, true>(v, ix, sa, sb, tb, magic);
+        else
+          acc += chunk_dot<N, false>(v, ix, sa, sb, tb, magic);
+      } else {
+        acc += chunk_dot<N, N == 1 && MODE == kOneG64>(v, ix, sa, sb, tb, magic);
+      }
       if (ci == cpl - 1) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
           const int rl = warp_row(warp, cj, nr);
           if (p.nslices == 1) {
-            p.y[r0 + rl] = __float2half_rn(acc);
+            *yrow = __float2half_rn(acc);
           } else {
             const float t = (sl ? part[rl] : 0.0f) + acc;
             if (sl == p.nslices - 1)
-              p.y[r0 + rl] = __float2half_rn(t);
+              *yrow = __float2half_rn(t);
             else
               part[rl] = t;
           }
@@ -475,12 +527,21 @@ int num_sms() {
   return g_num_sms[dev];
 }
 
-template <int N, bool G2>
-cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
+// One launch over `count` matrices that share x, cols and N (count <= kMaxSeg).
+template <int N, int MODE>
+cudaError_t launch_m1_n(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s) {
   using C = M1Cfg<N>;
-  const int chunks = (int)L.chunks;
-  if ((int64_t)L.rows * L.cstride >= (1ll << 31) || (int64_t)L.rows * L.gstride >= (1ll << 31))
-    return cudaErrorNotSupported;
+  const Layout& L0 = Ls[0];
+  const int chunks = (int)L0.chunks;
+  int64_t total_rows = 0;
+  for (int i = 0; i < count; ++i) {
+    if ((int64_t)Ls[i].rows * Ls[i].cstride >= (1ll << 31) ||
+        (int64_t)Ls[i].rows * Ls[i].gstride >= (1ll << 31))
+      return cudaErrorNotSupported;
+    total_rows += Ls[i].rows;
+  }
+  if (total_rows == 0) return cudaSuccess;
+  if (total_rows >= (1ll << 31)) return cudaErrorNotSupported;
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorNotSupported;
   const size_t ring = (size_t)kNW * kS * kStage;
@@ -490,22 +551,35 @@ cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   if (max_cpl < 1) return cudaErrorNotSupported;
   const int nslices = (chunks + 32 * max_cpl - 1) / (32 * max_cpl);
   const int cpl = (chunks + 32 * nslices - 1) / (32 * nslices);
-  int rows_per_cta = (L.rows + sms - 1) / sms;
+  const int rows = (int)total_rows;
+  int rows_per_cta = (rows + sms - 1) / sms;
   if (nslices > 1 && rows_per_cta > 1024) rows_per_cta = 1024;
-  const int grid = (L.rows + rows_per_cta - 1) / rows_per_cta;
+  const int grid = (rows + rows_per_cta - 1) / rows_per_cta;
 
   M1Params p;
-  p.vals = a.vals;
-  p.idx = a.idx;
-  p.sz = a.sz;
-  p.x = a.x;
-  p.y = a.y;
-  p.err = a.err;
-  p.rows = L.rows;
-  p.cols = L.cols;
-  p.gstride = (int)L.gstride;
-  p.cstride = (int)L.cstride;
-  p.gshift = L.group == 64 ? 6 : (L.group == 128 ? 7 : 8);
+  memset(&p, 0, sizeof p);
+  int row_begin = 0;
+  for (int i = 0; i < count; ++i) {
+    M1Seg& sg = p.seg[i];
+    sg.vals = as[i].vals;
+    sg.idx = as[i].idx;
+    sg.sz = as[i].sz;
+    sg.y = as[i].y;
+    sg.row_begin = row_begin;
+    sg.gstride = (int)Ls[i].gstride;
+    sg.gshift = Ls[i].group == 64 ? 6 : (Ls[i].group == 128 ? 7 : 8);
+    sg.g64 = N == 1 && Ls[i].group == 64;
+    row_begin += Ls[i].rows;
+  }
+  // empty matrices may sit anywhere in the list; unused entries start past
+  // the row space so the lookup never selects them
+  for (int i = count; i < kMaxSeg; ++i) p.seg[i].row_begin = rows;
+  p.nseg = count;
+  p.x = as[0].x;
+  p.err = as[0].err;
+  p.rows = rows;
+  p.cols = L0.cols;
+  p.cstride = (int)L0.cstride;
   p.chunks = chunks;
   p.rows_per_cta = rows_per_cta;
   p.cpl = cpl;
@@ -519,9 +593,8 @@ cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_m1<N, G2>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemLimit);
+    cudaError_t e = cudaFuncSetAttribute(k_m1<N, MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -535,15 +608,28 @@ cudaError_t launch_m1_n(const Layout& L, const RunArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_m1<N, G2>, p);
+  return cudaLaunchKernelEx(&cfg, k_m1<N, MODE>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_m1(const Layout& L, const RunArgs& a, cudaStream_t s) {
   if (a.m != 1 || L.rows == 0 || L.cols == 0) return cudaErrorNotSupported;
-  if (L.n_keep == 2) return launch_m1_n<2, false>(L, a, s);
-  return L.group == 64 ? launch_m1_n<1, true>(L, a, s) : launch_m1_n<1, false>(L, a, s);
+  if (L.n_keep == 2) return launch_m1_n<2, kOne>(&L, &a, 1, s);
+  return L.group == 64 ? launch_m1_n<1, kOneG64>(&L, &a, 1, s)
+                       : launch_m1_n<1, kOne>(&L, &a, 1, s);
 }
+
+cudaError_t launch_m1_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s) {
+  if (count < 1 || count > kMaxSeg) return cudaErrorNotSupported;
+  for (int i = 0; i < count; ++i)
+    if (as[i].m != 1 || Ls[i].cols != Ls[0].cols || Ls[i].n_keep != Ls[0].n_keep ||
+        Ls[i].cols == 0)
+      return cudaErrorNotSupported;
+  return Ls[0].n_keep == 2 ? launch_m1_n<2, kMany>(Ls, as, count, s)
+                           : launch_m1_n<1, kMany>(Ls, as, count, s);
+}
+
+int max_group() { return kMaxSeg; }
 
 }  // namespace sgemv

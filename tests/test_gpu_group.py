@@ -1,0 +1,101 @@
+"""Grouped run (several matrices sharing x) through the C ABI: every output
+equals the per-matrix run bit for bit and matches the oracle."""
+import numpy as np
+import pytest
+
+import synth
+from _check import check_y
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _mats(native, orc, specs, cols, max_m=1):
+    out = []
+    for i, (rows, n_keep, group) in enumerate(specs):
+        W = synth.weight_outliers(300 + i, rows, cols)
+        p = orc.pack(W, n_keep, group)
+        h = native.SparseGemv(rows, cols, n_keep, group, max_m=max_m)
+        h.import_canonical(p.vals, p.idx, p.scale, p.zero)
+        out.append((h, p))
+    return out
+
+
+def _ys(mats, m):
+    return [torch.full((m, h.rows), 9.0, dtype=torch.float16, device="cuda")
+            for h, _ in mats]
+
+
+@pytest.mark.parametrize("m", [1, 5])
+def test_group_matches_single_and_oracle(native, orc, m):
+    cols = 1536
+    specs = [(300, 1, 256), (129, 2, 128), (64, 1, 128), (1, 2, 64),
+             (257, 1, 64), (33, 2, 64), (200, 2, 256), (96, 1, 128),
+             (70, 2, 128), (5, 1, 64)]          # 10 > 8: two launches per N
+    mats = _mats(native, orc, specs, cols, max_m=8)
+    x = torch.from_numpy(synth.activations(41 + m, m, cols)).cuda()
+    ys = _ys(mats, m)
+    native.run_group([h for h, _ in mats], x, ys)
+    torch.cuda.synchronize()
+    for (h, p), y in zip(mats, ys):
+        single = torch.empty_like(y)
+        h.run(x, single)
+        torch.cuda.synchronize()
+        assert torch.equal(y, single)
+        ref = orc.matvec(p, x.cpu().numpy())
+        norms = np.abs(orc.dequant(p)).sum(axis=1)
+        check_y(orc, y.cpu().numpy(), ref, norms, f"group member {h.rows}x{cols}")
+        assert h.status() == 0
+
+
+def test_group_qkv_shapes(native, orc):
+    """The decoder layer's q/k/v (mixed N, g) and gate/up groups at full size."""
+    gvs = synth.config3()
+    for names in (("q", "k", "v"), ("gate", "up")):
+        sel = [g for g in gvs if g.name in names]
+        mats = []
+        for gv in sel:
+            W = gv.weight()
+            p = orc.pack(W, gv.n_keep, gv.group)
+            h = native.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group)
+            h.pack(W)
+            mats.append((h, p))
+        x = torch.from_numpy(sel[0].x(1)).cuda()
+        ys = _ys(mats, 1)
+        native.run_group([h for h, _ in mats], x, ys)
+        torch.cuda.synchronize()
+        for (h, p), y in zip(mats, ys):
+            single = torch.empty_like(y)
+            h.run(x, single)
+            torch.cuda.synchronize()
+            assert torch.equal(y, single)
+            rows = np.arange(0, h.rows, 37, dtype=np.int64)
+            ref = orc.matvec(p, x.cpu().numpy(), rows)
+            norms = np.array([np.abs(orc.dequant(p, int(r), 1)).sum() for r in rows])
+            check_y(orc, y.cpu().numpy()[:, rows], ref, norms, f"{names} {h.rows}")
+
+
+def test_group_edges(native, orc):
+    from sparse_weight_only_gb300 import SgemvError
+    cols = 512
+    mats = _mats(native, orc, [(0, 2, 64), (40, 1, 128), (0, 1, 64)], cols)
+    x = torch.from_numpy(synth.activations(7, 1, cols)).cuda()
+    ys = _ys(mats, 1)
+    native.run_group([h for h, _ in mats], x, ys)       # empty members skipped
+    torch.cuda.synchronize()
+    single = torch.empty_like(ys[1])
+    mats[1][0].run(x, single)
+    torch.cuda.synchronize()
+    assert torch.equal(ys[1], single)
+    native.run_group([], x, [])                          # count 0: no-op
+    other = _mats(native, orc, [(8, 2, 64)], 256)
+    with pytest.raises(SgemvError) as e:                 # cols differ
+        native.run_group([mats[1][0], other[0][0]], x,
+                         [ys[1], torch.empty((1, 8), dtype=torch.float16, device="cuda")])
+    assert e.value.code == native.SGEMV_ERR_ARG
+    with pytest.raises(SgemvError) as e:                 # m > max_m
+        native.run_group([mats[1][0]], torch.zeros((2, cols), dtype=torch.float16,
+                                                    device="cuda"),
+                         [torch.empty((2, 40), dtype=torch.float16, device="cuda")])
+    assert e.value.code == native.SGEMV_ERR_ARG
