@@ -37,7 +37,10 @@ namespace {
 
 constexpr int kW = 8;                 // warps per CTA
 constexpr int kRowsCta = 16 * kW;     // weight rows per CTA
-constexpr int kMaxSplit = 8;          // CTAs per cluster (portable limit)
+#ifndef SGEMV_MMA_MAXSPLIT
+#define SGEMV_MMA_MAXSPLIT 8
+#endif
+constexpr int kMaxSplit = SGEMV_MMA_MAXSPLIT;  // CTAs per cluster (portable limit 8)
 constexpr int kXBudget = 64 * 1024;   // bytes of staged x per CTA
 
 struct MmaParams {
@@ -243,13 +246,18 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
     const int r_lo = rank * kRowsCta / p.nsplit, r_hi = (rank + 1) * kRowsCta / p.nsplit;
     const int n_el = (r_hi - r_lo) * p.m;
     const int row0 = (blockIdx.x / p.nsplit) * kRowsCta;
+    const float* rp[kMaxSplit];
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q)
+      rp[q] = cluster.map_shared_rank(part, q < p.nsplit ? q : 0);
     for (int e = threadIdx.x; e < n_el; e += kW * 32) {
       const int lr = r_lo + e / p.m, mm = e % p.m;
+      float v[kMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kMaxSplit; ++q) v[q] = q < p.nsplit ? rp[q][lr * mp + mm] : 0.0f;
       float sum = 0.0f;
-      for (int q = 0; q < p.nsplit; ++q) {
-        const float* rp = cluster.map_shared_rank(part, q);
-        sum += rp[lr * mp + mm];
-      }
+#pragma unroll
+      for (int q = 0; q < kMaxSplit; ++q) sum += v[q];
       const int row = row0 + lr;
       if (row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(sum);
     }
@@ -261,7 +269,10 @@ template <int NT>
 cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms) {
   const int chunks = (int)L.chunks;
   const int ntiles = (L.rows + kRowsCta - 1) / kRowsCta;
-  int nsplit = (2 * sms + ntiles - 1) / ntiles;
+#ifndef SGEMV_MMA_CTAS_PER_SM
+#define SGEMV_MMA_CTAS_PER_SM 2
+#endif
+  int nsplit = (SGEMV_MMA_CTAS_PER_SM * sms + ntiles - 1) / ntiles;
   nsplit = max(1, min(kMaxSplit, min(nsplit, chunks)));
   const int split_chunks = (chunks + nsplit - 1) / nsplit;
   nsplit = (chunks + split_chunks - 1) / split_chunks;
@@ -293,6 +304,10 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
     cudaError_t e = cudaFuncSetAttribute(k_mma24<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
     if (e != cudaSuccess) return e;
+    if (kMaxSplit > 8) {
+      e = cudaFuncSetAttribute(k_mma24<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
