@@ -196,7 +196,8 @@ def read_traffic(kernel_tag: str):
     if not ent:
         return None
     from sparse_weight_only_gb300.build import _stamp
-    if ent.get("source_stamp") != _stamp():
+    files = ent.get("source_files")
+    if not files or ent.get("source_stamp") != _stamp(files):
         return None
     return ent
 

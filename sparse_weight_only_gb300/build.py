@@ -39,14 +39,20 @@ def sources() -> list[str]:
                   if f.endswith(".cu"))
 
 
-def _stamp() -> str:
+def _stamp(files: list[str] | None = None) -> str:
+    """Hash of the sources (all of csrc, or the named csrc files), the public
+    header and the compiler flags.  A record taken on one kernel (a profile's
+    traffic) names that kernel's files, so edits elsewhere keep it valid."""
     h = hashlib.sha256()
-    deps = sources() + sorted(
-        os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh"))
+    if files is None:
+        deps = sources() + sorted(
+            os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh"))
+    else:
+        deps = [os.path.join(CSRC, f) for f in files]
     deps.append(os.path.join(INCLUDE, "sgemv.h"))
     for p in deps:
         with open(p, "rb") as f:
-            h.update(p.encode() + b"\0" + f.read())
+            h.update(os.path.basename(p).encode() + b"\0" + f.read())
     h.update(" ".join(ARCH + NVCC_FLAGS).encode())
     return h.hexdigest()
 

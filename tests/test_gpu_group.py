@@ -27,9 +27,8 @@ def _ys(mats, m):
             for h, _ in mats]
 
 
-@pytest.mark.parametrize("m", [1, 5])
-def test_group_matches_single_and_oracle(native, orc, m):
-    cols = 1536
+@pytest.mark.parametrize("m,cols", [(1, 1536), (5, 1536), (1, 8192)])
+def test_group_matches_single_and_oracle(native, orc, m, cols):
     specs = [(300, 1, 256), (129, 2, 128), (64, 1, 128), (1, 2, 64),
              (257, 1, 64), (33, 2, 64), (200, 2, 256), (96, 1, 128),
              (70, 2, 128), (5, 1, 64)]          # 10 > 8: two launches per N

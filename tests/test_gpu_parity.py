@@ -58,6 +58,10 @@ SMALL = [  # rows, cols, n_keep, group, dist
     (300, 1024, 2, 64, "outliers"),
     (257, 2304, 2, 256, "normal"),
     (96, 4160, 1, 64, "outliers"),    # 1:4 ragged tail, K not a multiple of 128
+    (50, 8192, 1, 128, "normal"),     # longer rows: several chunks per lane
+    (40, 8192, 1, 256, "outliers"),
+    (24, 16384, 2, 128, "outliers"),  # rows longer than one K slice
+    (24, 16384, 1, 64, "normal"),
 ]
 
 
