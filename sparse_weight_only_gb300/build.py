@@ -53,7 +53,8 @@ def _stamp(files: list[str] | None = None) -> str:
     for p in deps:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode() + b"\0" + f.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    # flags without the machine-specific include path
+    h.update(" ".join(f for f in ARCH + NVCC_FLAGS if f != INCLUDE).encode())
     return h.hexdigest()
 
 

@@ -20,6 +20,11 @@
 //    4t..4t+3 of rows g (low half) and g + 8 (high half).
 //  * B (32 x 8): x rows staged in shared memory (padded rows, so ldmatrix
 //    reads are conflict-free), one ldmatrix.x4 per n-tile and k-tile.
+//  * weights: the CTA's 128 rows x K sub-slice (codes, positions and the
+//    sub-slice's scale/zero words) are copied into shared memory with
+//    cp.async, double-buffered across sub-slices; the first sub-slice is in
+//    flight while x is staged.  Warps read their rows from padded rows of
+//    the buffer (conflict-free).
 //  * scale: each k-tile lies inside one group; the MMA accumulates a group
 //    into a temporary that is scaled by s and added in fp32.
 //  * split-K across the CTAs of a thread-block cluster: every CTA writes its
@@ -41,7 +46,7 @@ constexpr int kRowsCta = 16 * kW;     // weight rows per CTA
 #define SGEMV_MMA_MAXSPLIT 8
 #endif
 constexpr int kMaxSplit = SGEMV_MMA_MAXSPLIT;  // CTAs per cluster (portable limit 8)
-constexpr int kXBudget = 64 * 1024;   // bytes of staged x per CTA
+constexpr size_t kSmemPerCta = 113 * 1024;  // two CTAs per SM
 
 struct MmaParams {
   const uint4* vals;
@@ -53,7 +58,8 @@ struct MmaParams {
   int m;
   int split_chunks;   // chunks per cluster rank
   int nsplit;         // cluster size
-  int sub_chunks;     // chunks of x staged at a time
+  int sub_chunks;     // chunks of weights and x staged at a time
+  int sub_groups;     // scale/zero words per row staged per sub-slice (bound)
 };
 
 // code (0..5) -> (a | b << 2): (0,1)=4 (0,2)=8 (0,3)=12 (1,2)=9 (1,3)=13 (2,3)=14
@@ -94,19 +100,35 @@ __device__ __forceinline__ void mma_sp(float (&c)[4], uint32_t a0, uint32_t a1, 
         "r"(meta));
 }
 
-__device__ __forceinline__ uint4 ld_nc16(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void* src) {
+  if (BYTES == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(BYTES)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint2 ld_nc8(const uint2* p) {
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
   uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-               : "=r"(v.x), "=r"(v.y)
-               : "l"(p));
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 
@@ -115,6 +137,45 @@ __device__ __forceinline__ void group_consts(uint32_t szw, float& s, uint32_t& z
   s = __half2float(__ushort_as_half((unsigned short)(szw & 0xFFFFu)));
   const uint32_t zz = __byte_perm(szw, 0u, 0x3232u);  // (z, z)
   asm("add.rn.f16x2 %0, %1, %2;" : "=r"(zc) : "r"(zz), "r"(0x54006400u));
+}
+
+// Shared-memory geometry of one weight buffer: the CTA's 128 rows x SC
+// chunks of a K sub-slice.  Row strides are padded by one element so that
+// the 8 rows a warp instruction reads fall in different banks.
+struct WGeom {
+  int sc;        // chunks per sub-slice
+  int gs;        // scale/zero words per row and sub-slice (upper bound)
+  int vst, ist, sst;          // row strides in bytes
+  int vals_off, idx_off, sz_off, bytes;
+  __host__ __device__ WGeom(int sc_, int gs_) : sc(sc_), gs(gs_) {
+    vst = sc * 16 + 16;
+    ist = sc * 8 + 8;
+    sst = (gs + 1) * 4;
+    vals_off = 0;
+    idx_off = kRowsCta * vst;
+    sz_off = idx_off + kRowsCta * ist;
+    bytes = (sz_off + kRowsCta * sst + 127) & ~127;
+  }
+};
+
+// Copies the weight block of rows [row0, row0 + 128) x chunks [cs, ce) and
+// the scale/zero words of groups [g0, g1] into a buffer; rows past the
+// matrix are skipped (their values are replaced when read).
+__device__ __forceinline__ void stage_weights(const MmaParams& p, const WGeom& W, uint32_t buf,
+                                              int row0, int cs, int ce, int g0, int g1) {
+  const int nc = ce - cs, ng = g1 - g0 + 1;
+  const int nrow = min(kRowsCta, p.rows - row0);
+  for (int i = threadIdx.x; i < nrow * nc; i += kW * 32) {
+    const int r = i / nc, cc = i - r * nc;
+    const size_t src = (size_t)(row0 + r) * p.cstride + cs + cc;
+    cp_async<16>(buf + W.vals_off + r * W.vst + cc * 16, p.vals + src);
+    cp_async<8>(buf + W.idx_off + r * W.ist + cc * 8, p.idx + src);
+  }
+  for (int i = threadIdx.x; i < nrow * ng; i += kW * 32) {
+    const int r = i / ng, gg = i - r * ng;
+    cp_async<4>(buf + W.sz_off + r * W.sst + gg * 4,
+                p.sz + (size_t)(row0 + r) * p.gstride + g0 + gg);
+  }
 }
 
 template <int NT>
@@ -126,15 +187,23 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   const int g = lane >> 2, t = lane & 3;
   const int mp = NT * 8;                       // padded activation rows
   const int xs_stride = p.sub_chunks * 64 + 8; // halves per staged x row
+  const WGeom W(p.sub_chunks, p.sub_groups);
+  // shared memory: x of the sub-slice | two weight buffers; after the main
+  // loop the partial tile for the cluster reduction reuses the front
   __half* xs = reinterpret_cast<__half*>(smem);
-  float* part = reinterpret_cast<float*>(smem + (size_t)mp * xs_stride * 2);
   const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(xs);
+  const int xs_bytes = (mp * xs_stride * 2 + 127) & ~127;
+  const uint32_t wbuf0 = xs_s + (uint32_t)xs_bytes;
+  float* part = reinterpret_cast<float*>(smem);
 
-  const int rowbase = (blockIdx.x / p.nsplit) * kRowsCta + warp * 16;
+  const int row0 = (blockIdx.x / p.nsplit) * kRowsCta;
+  const int rowbase = row0 + warp * 16;
   const int rg = rowbase + g, rg8 = rowbase + g + 8;
   const bool vg = rg < p.rows, vg8 = rg8 < p.rows;
+  const int lr_g = warp * 16 + g, lr_g8 = lr_g + 8;   // rows within the CTA
   const int c_begin = rank * p.split_chunks;
   const int c_end = min(p.chunks, c_begin + p.split_chunks);
+  const int nsub = c_end > c_begin ? (c_end - c_begin + p.sub_chunks - 1) / p.sub_chunks : 0;
 
   float acc[NT][4];
   float tmp[NT][4];
@@ -152,9 +221,26 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   // ldmatrix row address of this thread: matrix j = lane / 8, row lane % 8
   const uint32_t ld_base = xs_s + (uint32_t)(((lane & 7) * xs_stride + (lane >> 3) * 8) * 2);
 
-  for (int cs = c_begin; cs < c_end; cs += p.sub_chunks) {
+  // weights of the first sub-slice: in flight while x is staged
+  if (nsub > 0) {
+    const int ce = min(c_end, c_begin + p.sub_chunks);
+    stage_weights(p, W, wbuf0, row0, c_begin, ce, (c_begin * 64) >> p.gshift,
+                  (ce * 64 - 1) >> p.gshift);
+  }
+  cp_commit();
+
+  for (int sidx = 0; sidx < nsub; ++sidx) {
+    const int cs = c_begin + sidx * p.sub_chunks;
     const int ce = min(c_end, cs + p.sub_chunks);
-    __syncthreads();  // previous sub-slice fully consumed
+    const int g0 = (cs * 64) >> p.gshift;
+    const uint32_t wb = wbuf0 + (uint32_t)((sidx & 1) * W.bytes);
+    __syncthreads();  // previous sub-slice fully consumed: x and the other buffer are free
+    if (sidx + 1 < nsub) {
+      const int ns = ce, ne = min(c_end, ns + p.sub_chunks);
+      stage_weights(p, W, wbuf0 + (uint32_t)(((sidx + 1) & 1) * W.bytes), row0, ns, ne,
+                    (ns * 64) >> p.gshift, (ne * 64 - 1) >> p.gshift);
+    }
+    cp_commit();
     {
       // stage x[:, 64 cs .. 64 ce) (zero for padded rows)
       const int ncol = (ce - cs) * 64;
@@ -167,17 +253,19 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
         *reinterpret_cast<uint4*>(xs + row * xs_stride + c8 * 8) = q;
       }
     }
-    __syncthreads();
+    cp_wait<1>();     // this thread's copies of sub-slice sidx landed
+    __syncthreads();  // ... and every thread's; x is staged
     for (int c = cs; c < ce; ++c) {
+      const int cc = c - cs;
       uint4 v_g = make_uint4(0, 0, 0, 0), v_g8 = v_g;
       uint2 i_g = make_uint2(0, 0), i_g8 = i_g;
       if (vg) {
-        v_g = ld_nc16(p.vals + (size_t)rg * p.cstride + c);
-        i_g = ld_nc8(p.idx + (size_t)rg * p.cstride + c);
+        v_g = lds128(wb + W.vals_off + lr_g * W.vst + cc * 16);
+        i_g = lds64(wb + W.idx_off + lr_g * W.ist + cc * 8);
       }
       if (vg8) {
-        v_g8 = ld_nc16(p.vals + (size_t)rg8 * p.cstride + c);
-        i_g8 = ld_nc8(p.idx + (size_t)rg8 * p.cstride + c);
+        v_g8 = lds128(wb + W.vals_off + lr_g8 * W.vst + cc * 16);
+        i_g8 = lds64(wb + W.idx_off + lr_g8 * W.ist + cc * 8);
       }
 #pragma unroll
       for (int kt = 0; kt < 2; ++kt) {
@@ -194,8 +282,8 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
             }
           }
           cur_group = G;
-          const uint32_t w_g = vg ? p.sz[(size_t)rg * p.gstride + G] : 0x3C00u;
-          const uint32_t w_g8 = vg8 ? p.sz[(size_t)rg8 * p.gstride + G] : 0x3C00u;
+          const uint32_t w_g = vg ? lds32(wb + W.sz_off + lr_g * W.sst + (G - g0) * 4) : 0x3C00u;
+          const uint32_t w_g8 = vg8 ? lds32(wb + W.sz_off + lr_g8 * W.sst + (G - g0) * 4) : 0x3C00u;
           group_consts(w_g, s_g, zc_g);
           group_consts(w_g8, s_g8, zc_g8);
         }
@@ -209,7 +297,7 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
         const uint32_t cw_g = kt ? i_g.y : i_g.x, cw_g8 = kt ? i_g8.y : i_g8.x;
         const uint32_t sh = (t & 1) * 16;
         const uint32_t meta = meta16(cw_g >> sh) | (meta16(cw_g8 >> sh) << 16);
-        const uint32_t kofs = (uint32_t)(((c - cs) * 64 + kt * 32) * 2);
+        const uint32_t kofs = (uint32_t)((cc * 64 + kt * 32) * 2);
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           uint32_t b0, b1, b2, b3;
@@ -228,10 +316,11 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
       acc[n][3] = fmaf(s_g8, tmp[n][3], acc[n][3]);
     }
   }
+  cp_wait<0>();
+  __syncthreads();  // every warp is done with x and the buffers: part reuses them
 
   // ---- split-K reduction across the cluster (rank order, deterministic)
   // part: [kRowsCta][mp] fp32 of this CTA
-  const int lr_g = warp * 16 + g, lr_g8 = lr_g + 8;
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
     const int mc = n * 8 + 2 * t;
@@ -245,7 +334,6 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
     // rank k finishes rows [k * kRowsCta / nsplit, (k+1) * kRowsCta / nsplit)
     const int r_lo = rank * kRowsCta / p.nsplit, r_hi = (rank + 1) * kRowsCta / p.nsplit;
     const int n_el = (r_hi - r_lo) * p.m;
-    const int row0 = (blockIdx.x / p.nsplit) * kRowsCta;
     const float* rp[kMaxSplit];
 #pragma unroll
     for (int q = 0; q < kMaxSplit; ++q)
@@ -265,6 +353,16 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   cluster.sync();  // no CTA leaves while its partial tile is being read
 }
 
+// Shared memory of a launch with sub-slices of `sc` chunks.
+size_t mma_smem(int nt, int sc, int group) {
+  const int mp = nt * 8;
+  const WGeom W(sc, (sc * 64 + group - 1) / group + 1);
+  const size_t xs = ((size_t)mp * (sc * 64 + 8) * 2 + 127) & ~(size_t)127;
+  const size_t main = xs + 2 * (size_t)W.bytes;
+  const size_t red = (size_t)kRowsCta * mp * 4;
+  return main > red ? main : red;
+}
+
 template <int NT>
 cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms) {
   const int chunks = (int)L.chunks;
@@ -272,14 +370,16 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
 #ifndef SGEMV_MMA_CTAS_PER_SM
 #define SGEMV_MMA_CTAS_PER_SM 2
 #endif
-  int nsplit = (SGEMV_MMA_CTAS_PER_SM * sms + ntiles - 1) / ntiles;
+  // as many K splits as keep every CTA resident in one wave
+  int nsplit = (SGEMV_MMA_CTAS_PER_SM * sms) / ntiles;
   nsplit = max(1, min(kMaxSplit, min(nsplit, chunks)));
   const int split_chunks = (chunks + nsplit - 1) / nsplit;
   nsplit = (chunks + split_chunks - 1) / split_chunks;
-  // x staged per sub-slice: mp rows x (64 sub + 8) halves within budget
-  const int mp = NT * 8;
-  int sub = (kXBudget / (mp * 2) - 8) / 64;
-  sub = max(1, min(sub, split_chunks));
+  // sub-slices: as many chunks as fit two CTAs per SM
+  int sub = min(split_chunks, 64);
+  while (sub > 1 && mma_smem(NT, sub, L.group) > kSmemPerCta) sub = (sub + 1) / 2;
+  const size_t smem = mma_smem(NT, sub, L.group);
+  if (smem > 227 * 1024) return cudaErrorNotSupported;
   MmaParams p;
   p.vals = a.vals;
   p.idx = a.idx;
@@ -296,7 +396,7 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
   p.split_chunks = split_chunks;
   p.nsplit = nsplit;
   p.sub_chunks = sub;
-  const size_t smem = (size_t)mp * (sub * 64 + 8) * 2 + (size_t)kRowsCta * mp * 4;
+  p.sub_groups = (sub * 64 + L.group - 1) / L.group + 1;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
