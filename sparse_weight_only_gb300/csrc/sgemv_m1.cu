@@ -89,15 +89,6 @@ struct M1Params {
   int cpl;
 };
 
-// Matrix holding row `row` of the launch's row space (warp-uniform).
-__device__ __forceinline__ int find_seg(const M1Params& p, int row) {
-  int s = 0;
-#pragma unroll
-  for (int i = 1; i < kMaxSeg; ++i)
-    if (i < p.nseg && row >= p.seg[i].row_begin) s = i;
-  return s;
-}
-
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -129,11 +120,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 __device__ __forceinline__ uint2 lds64(uint32_t a) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 
@@ -254,94 +240,97 @@ __device__ __forceinline__ float chunk_dot(const uint4& v, const uint2& ix,
   }
 }
 
-// Local row (within the CTA's block of nr rows) of a warp's j-th row.  With
-// SGEMV_M1_CONSEC each warp takes a contiguous run of rows, so its copies
-// walk memory sequentially; otherwise rows interleave across warps.
-#ifdef SGEMV_M1_CONSEC
-__device__ __forceinline__ int warp_row(int warp, int j, int nr) {
-  return warp * ((nr + kNW - 1) / kNW) + j;
-}
-__device__ __forceinline__ int warp_nrows(int warp, int nr) {
-  const int q = (nr + kNW - 1) / kNW;
-  return max(0, min(q, nr - warp * q));
-}
-#else
-__device__ __forceinline__ int warp_row(int warp, int j, int) { return warp + kNW * j; }
+// Rows of a CTA interleave over its warps: the warp's j-th row is local row
+// warp + kNW j.
 __device__ __forceinline__ int warp_nrows(int warp, int nr) {
   return warp < nr ? (nr - warp + kNW - 1) / kNW : 0;
 }
-#endif
 
-// Position of a warp in its item sequence: K slice, row of the warp, chunk
-// slot.  Item k of a warp is the slot'th group of 32 chunks of its j'th row
-// in slice sl.
 // MODE of a launch: kOne = one matrix, groups of 64 columns not split
 // across chunks; kOneG64 = one 1:4 matrix with 64-column groups (two groups
 // per chunk); kMany = several matrices, the split decided per row.
 constexpr int kOne = 0, kOneG64 = 1, kMany = 2;
 
+// Matrix of launch row `row`, searched forward from `seg` (a warp visits its
+// rows in increasing order within a K slice).
 template <int MODE>
-struct Cursor {
-  int sl, j, i;
-  int c0, nch, cpl;
-  // the row of item (sl, j): its matrix's rows of nibbles, codes, scales
-  const uint4* vrow;
-  const uint2* irow;
-  const uint32_t* srow;
-  int gshift, g64;
-  __device__ __forceinline__ void set_row(const M1Params& p, int row) {
-    const M1Seg& sg = p.seg[MODE == kMany ? find_seg(p, row) : 0];
+__device__ __forceinline__ int seg_from(const M1Params& p, int seg, int row) {
+  if (MODE == kMany)
+    while (seg + 1 < p.nseg && row >= p.seg[seg + 1].row_begin) ++seg;
+  return MODE == kMany ? seg : 0;
+}
+
+// The copy side of a warp's ring: walks the warp's items (K slices in
+// order; in a slice the warp's rows in order; in a row `ipr` items of 32
+// chunks, item i holding chunk c0 + 32 i + lane of each lane) with
+// per-lane pointers that advance by one item per step.
+template <int N, int MODE>
+struct Producer {
+  int sl, j;           // K slice, row ordinal of the warp
+  int left;            // items left in the current row
+  int vleft;           // of them, items in which this lane holds a chunk
+  int seg;             // matrix of the current row
+  int sstep;           // scale/zero words between a lane's consecutive items
+  bool g64;            // two scale/zero words per chunk
+  const uint4* vp;     // this lane's next chunk: nibbles, codes, scale/zero
+  const uint2* ip;
+  const uint32_t* sp;
+  int c0, ipr, lane_items;
+
+  __device__ __forceinline__ void set_row(const M1Params& p, int row, int lane) {
+    using C = M1Cfg<N>;
+    seg = seg_from<MODE>(p, seg, row);
+    const M1Seg& sg = p.seg[seg];
     const int lr = row - sg.row_begin;
-    vrow = sg.vals + (size_t)lr * p.cstride;
-    irow = sg.idx + (size_t)lr * p.cstride;
-    srow = sg.sz + (size_t)lr * sg.gstride;
-    gshift = sg.gshift;
-    g64 = MODE == kMany ? sg.g64 : (MODE == kOneG64);
+    const int ch = c0 + lane;
+    vp = sg.vals + (size_t)lr * p.cstride + ch;
+    ip = sg.idx + (size_t)lr * p.cstride + ch;
+    sp = sg.sz + (size_t)lr * sg.gstride + ((ch * C::CPC) >> sg.gshift);
+    sstep = (32 * C::CPC) >> sg.gshift;
+    g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
+    left = ipr;
+    vleft = lane_items;
   }
-  __device__ __forceinline__ void start(const M1Params& p, int s, int r0, int warp, int nr) {
-    sl = s;
+  __device__ __forceinline__ void start_slice(const M1Params& p, int r0, int warp, int lane) {
+    c0 = sl * p.slice_chunks;
+    const int nch = min(p.slice_chunks, p.chunks - c0);
+    ipr = (nch + 31) >> 5;
+    lane_items = nch > lane ? (nch - lane + 31) >> 5 : 0;
     j = 0;
-    i = 0;
-    c0 = s * p.slice_chunks;
-    nch = min(p.slice_chunks, p.chunks - c0);
-    cpl = (nch + 31) >> 5;
-    if (warp_nrows(warp, nr) > 0) set_row(p, r0 + warp_row(warp, 0, nr));
+    seg = 0;
+    set_row(p, r0 + warp, lane);
   }
-  // false once past the last slice
-  __device__ __forceinline__ bool next(const M1Params& p, int nrw, int r0, int warp, int nr) {
-    if (++i < cpl) return true;
-    i = 0;
+  // Copies this lane's part of the next item into `stage`: 16 bytes of
+  // nibbles, 8 bytes of codes and the scale/zero word(s), each into a region
+  // only this lane reads.  A lane without a chunk in the item copies
+  // nothing (its result is discarded).
+  __device__ __forceinline__ void issue(uint32_t s16, uint32_t s8) const {
+    if (vleft > 0) {
+      cp_async<16>(s16, vp);
+      cp_async<8>(s8 + kIdxOff, ip);
+      if (g64)
+        cp_async<8>(s8 + kSzOff, sp);
+      else
+        cp_async<4>(s8 + kSzOff, sp);
+    }
+  }
+  // false once past the warp's last item
+  __device__ __forceinline__ bool advance(const M1Params& p, int r0, int warp, int nrw,
+                                          int lane) {
+    vp += 32;
+    ip += 32;
+    sp += sstep;
+    --vleft;
+    if (--left > 0) return true;
     if (++j < nrw) {
-      set_row(p, r0 + warp_row(warp, j, nr));
+      set_row(p, r0 + warp + kNW * j, lane);
       return true;
     }
-    if (sl + 1 >= p.nslices) {
-      ++sl;
-      return false;
-    }
-    start(p, sl + 1, r0, warp, nr);
+    if (++sl >= p.nslices) return false;
+    start_slice(p, r0, warp, lane);
     return true;
   }
 };
-
-// Copies this lane's part of item `c` into the stage with per-lane
-// asynchronous copies: its 16 bytes of nibbles, 8 bytes of codes and its
-// scale/zero word(s), each into a region of the stage only this lane reads.
-// Lanes past a ragged slice copy nothing (their results are discarded).
-template <int N, int MODE>
-__device__ __forceinline__ void issue_item(const Cursor<MODE>& c, int lane, uint32_t stage) {
-  using C = M1Cfg<N>;
-  const int ch = c.c0 + 32 * c.i + lane;
-  if (ch < c.c0 + c.nch) {
-    cp_async<16>(stage + 16 * lane, c.vrow + ch);
-    cp_async<8>(stage + kIdxOff + 8 * lane, c.irow + ch);
-    const uint32_t* sp = c.srow + ((ch * C::CPC) >> c.gshift);
-    if (N == 1 && (MODE == kOneG64 || (MODE == kMany && c.g64)))
-      cp_async<8>(stage + kSzOff + 8 * lane, sp);
-    else
-      cp_async<4>(stage + kSzOff + 8 * lane, sp);
-  }
-}
 
 template <int N, int MODE>
 __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
@@ -379,13 +368,18 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   for (int b = 16 * lane; b < kS * kStage; b += 16 * 32)
     asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(my_ring + b), "r"(0u) : "memory");
   __syncwarp();
-  Cursor<MODE> prod;
-  prod.start(p, 0, r0, warp, nr);
+  // this lane's regions of ring stage 0 (nibbles; codes and scale/zero)
+  const uint32_t ring16 = my_ring + 16 * lane, ring8 = my_ring + 8 * lane;
+  Producer<N, MODE> prod;
   bool more = nrw > 0;
+  if (more) {
+    prod.sl = 0;
+    prod.start_slice(p, r0, warp, lane);
+  }
   for (int st = 0; st < kS; ++st) {
     if (more) {
-      issue_item<N, MODE>(prod, lane, my_ring + st * kStage);
-      more = prod.next(p, nrw, r0, warp, nr);
+      prod.issue(ring16 + st * kStage, ring8 + st * kStage);
+      more = prod.advance(p, r0, warp, nrw, lane);
     }
     cp_commit();
   }
@@ -393,12 +387,12 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   pdl_wait();
   pdl_launch_dependents();
 
-  int consumed = 0;
+  int st = 0;   // ring stage of the next item to compute
   for (int sl = 0; sl < p.nslices; ++sl) {
     const int c0 = sl * p.slice_chunks;
     const int nch = min(p.slice_chunks, p.chunks - c0);
-    const int cpl = (nch + 31) >> 5;
-    const int nitems = nrw * cpl;
+    const int ipr = (nch + 31) >> 5;                 // items per row
+    const int lane_items = nch > lane ? (nch - lane + 31) >> 5 : 0;
     __syncthreads();  // the previous slice's table is no longer read
 
     // ---- stage x of the slice (binary16, zero past cols), padded per chunk
@@ -422,7 +416,7 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
     {
       const int l = threadIdx.x & 31;
       const uint32_t colbase = smem_s + (uint32_t)((l >> 4) * S) * 128u + (l & 15) * 8u;
-      for (int u_it = warp; u_it < cpl * kUnitsPerChunk; u_it += kNW) {
+      for (int u_it = warp; u_it < ipr * kUnitsPerChunk; u_it += kNW) {
         const int i = u_it / kUnitsPerChunk, u = u_it % kUnitsPerChunk;
         const int cl = l + 32 * i;
         float xv[C::UC];
@@ -450,62 +444,54 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
     }
     __syncthreads();
 
-    // ---- stream the rows of this slice
-    int ci = 0, cj = 0;  // (chunk slot, row) of the item being computed
-    float acc = 0.0f;
-    __half* yrow = nullptr;  // output element of the current row
-    bool g64 = false;
-    for (int k = 0; k < nitems; ++k, ++consumed) {
-      if (ci == 0) {
-        const int row = r0 + warp_row(warp, cj, nr);
-        const M1Seg& sg = p.seg[MODE == kMany ? find_seg(p, row) : 0];
-        yrow = sg.y + (row - sg.row_begin);
-        g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
-      }
-      const int st = consumed % kS;
-      const uint32_t stage = my_ring + st * kStage;
-      cp_wait<kS - 1>();   // this lane's copies of item `consumed` landed
-      const bool valid = lane + 32 * ci < nch;
-      const uint4 v = lds128(stage + 16 * lane);
-      const uint2 ix = lds64(stage + kIdxOff + 8 * lane);
-      const uint2 s2 = lds64(stage + kSzOff + 8 * lane);
-      const uint32_t sa = valid ? s2.x : 0u;   // ragged slice: zero contribution
-      const uint32_t sb = valid ? s2.y : 0u;
-      // refill the stage this lane just read with item consumed + kS
-      if (more) {
-        issue_item<N, MODE>(prod, lane, stage);
-        more = prod.next(p, nrw, r0, warp, nr);
-      }
-      cp_commit();
-      const uint32_t tb = lane_base + ci * kChunkSlotBytes;
-      if constexpr (N == 1 && MODE == kMany) {
-        if (g64)
-          acc += chunk_dot<N, true>(v, ix, sa, sb, tb, magic);
-        else
-          acc += chunk_dot<N, false>(v, ix, sa, sb, tb, magic);
-      } else {
-        acc += chunk_dot<N, N == 1 && MODE == kOneG64>(v, ix, sa, sb, tb, magic);
-      }
-      if (ci == cpl - 1) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-          const int rl = warp_row(warp, cj, nr);
-          if (p.nslices == 1) {
-            *yrow = __float2half_rn(acc);
-          } else {
-            const float t = (sl ? part[rl] : 0.0f) + acc;
-            if (sl == p.nslices - 1)
-              *yrow = __float2half_rn(t);
-            else
-              part[rl] = t;
-          }
+    // ---- stream the warp's rows of this slice
+    int seg = 0;
+    for (int j = 0; j < nrw; ++j) {
+      const int lr = warp + kNW * j;
+      const int row = r0 + lr;
+      seg = seg_from<MODE>(p, seg, row);
+      const M1Seg& sg = p.seg[seg];
+      const bool g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
+      float acc = 0.0f;
+      uint32_t tb = lane_base;   // table slot of the item's chunk
+      for (int ci = 0; ci < ipr; ++ci, tb += kChunkSlotBytes) {
+        const uint32_t so = (uint32_t)(st * kStage);
+        cp_wait<kS - 1>();   // this lane's copies of this item landed
+        const bool valid = ci < lane_items;
+        const uint4 v = lds128(ring16 + so);
+        const uint2 ix = lds64(ring8 + so + kIdxOff);
+        const uint2 s2 = lds64(ring8 + so + kSzOff);
+        const uint32_t sa = valid ? s2.x : 0u;   // ragged slice: zero contribution
+        const uint32_t sb = valid ? s2.y : 0u;
+        // refill the stage this lane just read with the item kS ahead
+        if (more) {
+          prod.issue(ring16 + so, ring8 + so);
+          more = prod.advance(p, r0, warp, nrw, lane);
         }
-        acc = 0.0f;
-        ci = 0;
-        ++cj;
-      } else {
-        ++ci;
+        cp_commit();
+        st = st + 1 == kS ? 0 : st + 1;
+        if constexpr (N == 1 && MODE == kMany) {
+          if (g64)
+            acc += chunk_dot<N, true>(v, ix, sa, sb, tb, magic);
+          else
+            acc += chunk_dot<N, false>(v, ix, sa, sb, tb, magic);
+        } else {
+          acc += chunk_dot<N, N == 1 && MODE == kOneG64>(v, ix, sa, sb, tb, magic);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) {
+        __half* yrow = sg.y + (row - sg.row_begin);
+        if (p.nslices == 1) {
+          *yrow = __float2half_rn(acc);
+        } else {
+          const float t = (sl ? part[lr] : 0.0f) + acc;
+          if (sl == p.nslices - 1)
+            *yrow = __float2half_rn(t);
+          else
+            part[lr] = t;
+        }
       }
     }
   }
