@@ -41,7 +41,10 @@ namespace {
 #ifndef SGEMV_M1_S
 #define SGEMV_M1_S 2
 #endif
-constexpr int kNT = 512;            // threads per CTA (one CTA per SM)
+#ifndef SGEMV_M1_NT
+#define SGEMV_M1_NT 512
+#endif
+constexpr int kNT = SGEMV_M1_NT;    // threads per CTA (one CTA per SM)
 constexpr int kNW = kNT / 32;
 constexpr int kS = SGEMV_M1_S;      // ring stages per warp (2 measured best)
 constexpr int kStage = 1024;        // bytes per stage
@@ -103,6 +106,21 @@ __device__ __forceinline__ void cp_async(uint32_t dst, const void* src) {
   else
     asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(BYTES)
                  : "memory");
+}
+// The same copy, issued only where `on` is set (a predicated instruction,
+// so lanes without a chunk need no divergent branch).
+template <int BYTES>
+__device__ __forceinline__ void cp_async_if(bool on, uint32_t dst, const void* src) {
+  if (BYTES == 16)
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %2, 0; @p cp.async.cg.shared.global [%0], [%1], 16; }" ::"r"(dst),
+        "l"(src), "r"((int)on)
+        : "memory");
+  else
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %2, 0; @p cp.async.ca.shared.global [%0], [%1], %3; }" ::"r"(dst),
+        "l"(src), "r"((int)on), "n"(BYTES)
+        : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -277,6 +295,9 @@ struct Producer {
   const uint32_t* sp;
   int c0, ipr, lane_items;
 
+  int vstep, sstep_row;   // pointer steps from the end of a row to the next row
+  int next_begin;          // first launch row of the next matrix (kMany)
+
   __device__ __forceinline__ void set_row(const M1Params& p, int row, int lane) {
     using C = M1Cfg<N>;
     seg = seg_from<MODE>(p, seg, row);
@@ -288,6 +309,9 @@ struct Producer {
     sp = sg.sz + (size_t)lr * sg.gstride + ((ch * C::CPC) >> sg.gshift);
     sstep = (32 * C::CPC) >> sg.gshift;
     g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
+    vstep = kNW * p.cstride - 32 * ipr;
+    sstep_row = kNW * sg.gstride - sstep * ipr;
+    next_begin = MODE == kMany && seg + 1 < p.nseg ? p.seg[seg + 1].row_begin : 0x7fffffff;
     left = ipr;
     vleft = lane_items;
   }
@@ -305,14 +329,13 @@ struct Producer {
   // only this lane reads.  A lane without a chunk in the item copies
   // nothing (its result is discarded).
   __device__ __forceinline__ void issue(uint32_t s16, uint32_t s8) const {
-    if (vleft > 0) {
-      cp_async<16>(s16, vp);
-      cp_async<8>(s8 + kIdxOff, ip);
-      if (g64)
-        cp_async<8>(s8 + kSzOff, sp);
-      else
-        cp_async<4>(s8 + kSzOff, sp);
-    }
+    const bool on = vleft > 0;
+    cp_async_if<16>(on, s16, vp);
+    cp_async_if<8>(on, s8 + kIdxOff, ip);
+    if (g64)
+      cp_async_if<8>(on, s8 + kSzOff, sp);
+    else
+      cp_async_if<4>(on, s8 + kSzOff, sp);
   }
   // false once past the warp's last item
   __device__ __forceinline__ bool advance(const M1Params& p, int r0, int warp, int nrw,
@@ -323,7 +346,16 @@ struct Producer {
     --vleft;
     if (--left > 0) return true;
     if (++j < nrw) {
-      set_row(p, r0 + warp + kNW * j, lane);
+      const int row = r0 + warp + kNW * j;
+      if (row < next_begin) {   // same matrix: step the pointers
+        vp += vstep;
+        ip += vstep;
+        sp += sstep_row;
+        left = ipr;
+        vleft = lane_items;
+      } else {
+        set_row(p, row, lane);
+      }
       return true;
     }
     if (++sl >= p.nslices) return false;
