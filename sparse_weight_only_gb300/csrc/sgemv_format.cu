@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict_
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       vw |= (uint32_t)(q[t][0] | (q[t][1] << 4)) << (8 * t);
-      iw |= (uint32_t)pair24_code(pos[t][0], pos[t][1]) << (4 * t);
+      iw |= (uint32_t)(pos[t][0] | (pos[t][1] << 2)) << (4 * t);
     }
     *reinterpret_cast<uint32_t*>(vals + r * vrow + 4 * k) = vw;
     *reinterpret_cast<uint16_t*>(idx + r * irow + 2 * k) = (uint16_t)iw;
@@ -182,16 +182,18 @@ __global__ void k_canon_to_device(Layout L, const uint8_t* __restrict__ cvals,
     const int64_t o = 8 * c + b;
     uint8_t byte = o < L.idx_row ? isrc[o] : 0;
     if constexpr (N == 2) {
+      // two quads per byte, (a | b << 2) in each nibble; the positions must
+      // ascend (a rejected byte becomes positions (0, 1), and pack fails)
       if (o < L.idx_row) {
-        // two quads per byte: (a | b << 2) in each nibble -> six-way code
-        uint8_t out = 0;
         for (int h = 0; h < 2; ++h) {
           const int nib = (byte >> (4 * h)) & 0xF;
-          const int code = pair24_code(nib & 3, nib >> 2);
-          if (code < 0) set_err(err, kDevErrBadIndex);
-          out |= (uint8_t)((code < 0 ? 0 : code) << (4 * h));
+          if ((nib & 3) >= (nib >> 2)) {
+            set_err(err, kDevErrBadIndex);
+            byte = (uint8_t)((byte & ~(0xF << (4 * h))) | (0x4 << (4 * h)));
+          }
         }
-        byte = out;
+      } else {
+        byte = 0x44;   // padding chunk: zero codes at positions (0, 1)
       }
     }
     idst[b] = byte;
@@ -239,17 +241,7 @@ __global__ void k_device_to_canon(Layout L, const uint8_t* __restrict__ vals,
   for (int b = 0; b < 8; ++b) {
     const int64_t o = 8 * c + b;
     if (o >= L.idx_row) continue;
-    uint8_t byte = isrc[b];
-    if constexpr (N == 2) {
-      uint8_t out = 0;
-      for (int h = 0; h < 2; ++h) {
-        const int code = (byte >> (4 * h)) & 0xF;
-        const int cc = code < 6 ? code : 0;
-        out |= (uint8_t)((pair24_a(cc) | (pair24_b(cc) << 2)) << (4 * h));
-      }
-      byte = out;
-    }
-    idst[o] = byte;
+    idst[o] = isrc[b];
   }
 }
 

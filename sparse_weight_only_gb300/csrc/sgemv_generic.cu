@@ -41,9 +41,8 @@ k_generic(Layout L, RunArgs a) {
         int64_t col[2];
         if (N == 2) {
           const int64_t quad = kUnitsPerChunk * c + u;
-          const int cc = code < 6 ? (int)code : 0;
-          col[0] = 4 * quad + pair24_a(cc);
-          col[1] = 4 * quad + pair24_b(cc);
+          col[0] = 4 * quad + (code & 3u);
+          col[1] = 4 * quad + (code >> 2);
         } else {
           const int64_t quad = 2 * (kUnitsPerChunk * c + u);
           col[0] = 4 * quad + (code & 3u);

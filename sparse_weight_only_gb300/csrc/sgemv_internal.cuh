@@ -9,14 +9,12 @@
 //            so that every row of `idx` starts on a 16-byte boundary.
 //   vals   : 16 bytes per chunk, identical to the canonical nibble order
 //            (kept weight i of the chunk at bits 4*(i%8) of 32-bit word i/8).
-//   idx    : 8 bytes per chunk; pair unit u's 4-bit code at bits 4*(u%8) of
-//            32-bit word u/8.
-//              N = 2: unit u is quad 16*chunk + u; its two ascending
-//                     positions (a, b) are stored as one of six codes,
-//                     kPair24 below;
-//              N = 1: unit u is quads (32*chunk + 2u, 32*chunk + 2u + 1);
-//                     code = a | b << 2 with a, b their positions (this is
-//                     the canonical bit order unchanged).
+//   idx    : 8 bytes per chunk, the canonical bits unchanged: pair unit u's
+//            4-bit field a | b << 2 at bits 4*(u%8) of 32-bit word u/8.
+//              N = 2: unit u is quad 16*chunk + u with ascending positions
+//                     a < b (one of six fields);
+//              N = 1: unit u is quads (32*chunk + 2u, 32*chunk + 2u + 1),
+//                     a and b their positions.
 //   sz     : 4 bytes per (row, group): binary16 scale in the low half,
 //            binary16 zero in the high half; rows padded with zero words to
 //            a multiple of 4 groups (16-byte aligned rows).
@@ -32,19 +30,6 @@ namespace sgemv {
 
 constexpr int kChunkKept = 32;   // kept weights per chunk
 constexpr int kUnitsPerChunk = 16;
-
-// Six ascending position pairs of a 2:4 quad, in code order.
-// code 0:(0,1) 1:(0,2) 2:(0,3) 3:(1,2) 4:(1,3) 5:(2,3)
-__host__ __device__ constexpr int pair24_a(int code) {
-  return code < 3 ? 0 : (code < 5 ? 1 : 2);
-}
-__host__ __device__ constexpr int pair24_b(int code) {
-  return code == 0 ? 1 : (code == 1 ? 2 : (code == 2 ? 3 : (code == 3 ? 2 : 3)));
-}
-// Inverse: (a | b << 2) -> code, or -1 when a >= b.
-__host__ __device__ constexpr int pair24_code(int a, int b) {
-  return a >= b ? -1 : (a == 0 ? b - 1 : (a == 1 ? b + 1 : 5));
-}
 
 struct Layout {
   int rows, cols, n_keep, group;

@@ -17,8 +17,9 @@
 //    the previous kernel.  (Per-warp bulk TMA copies of the same stages were
 //    measured slower: the items are 128-512 B, too small for the TMA unit.)
 //  * Pair tables of x in shared memory.  A "pair unit" is two kept weights
-//    whose columns are fixed by one 4-bit code (2:4: the quad's two
-//    positions, 6 codes; 1:4: two adjacent quads' positions, 16 codes).  For
+//    whose columns are fixed by one stored 4-bit position field (2:4: the
+//    quad's two positions, 6 values; 1:4: two adjacent quads' positions, 16
+//    values).  For
 //    every unit the table holds all candidate (x_first, x_second) pairs as
 //    fp32, so one 8-byte shared load fetches both activations already
 //    widened.  Each lane owns a private bank column (8 bytes of every
@@ -53,16 +54,29 @@ constexpr int kSzOff = 768;         // scale/zero words after the codes
 constexpr int kSmemLimit = 227 * 1024;
 constexpr uint32_t kTabAlign = 2048;
 
+// Pair-table geometry.  A unit's code indexes its entries at a 128-byte
+// stride (one 8-byte pair per lane of a half-warp).  1:4: 16 codes, 16
+// entries per unit.  2:4: the code is the stored position nibble a | b << 2,
+// one of {4, 8, 9, 12, 13, 14}; entries sit at (code - 4) from the unit's
+// base with units 7 entries apart -- the six codes are distinct mod 7, so
+// units interleave without overlap (112 slots per chunk, padded to 128).
 template <int N>
 struct M1Cfg {
-  static constexpr int E = N == 2 ? 6 : 16;          // pairs per unit
+  static constexpr int E = N == 2 ? 7 : 16;          // unit stride in entries
+  static constexpr int OFF0 = N == 2 ? -4 * 128 : 0; // entry of code 0 from the unit base
+  static constexpr int SLOTS = N == 2 ? 128 : 256;   // entries per chunk (a multiple of 16)
   static constexpr int CPC = N == 2 ? 64 : 128;      // dense columns per chunk
   static constexpr int UC = N == 2 ? 4 : 8;          // dense columns per unit
   static constexpr int XPAD = CPC + 2;               // staged x per chunk (halves)
   // shared bytes per chunk-per-lane of a K slice
-  static constexpr int TAB_PER_CPL = 32 * kUnitsPerChunk * E * 8;
+  static constexpr int TAB_PER_CPL = 32 * SLOTS * 8;
   static constexpr int X_PER_CPL = 32 * XPAD * 2;
 };
+
+// The six position nibbles a | b << 2 (a < b) of a 2:4 quad.
+__device__ __forceinline__ constexpr int quad24_nibble(int e) {
+  return e == 0 ? 0x4 : e == 1 ? 0x8 : e == 2 ? 0xC : e == 3 ? 0x9 : e == 4 ? 0xD : 0xE;
+}
 
 // One packed matrix of a launch.  A launch covers up to kMaxSeg matrices
 // that share x (and N): their rows are concatenated into one row space.
@@ -182,7 +196,7 @@ __device__ __forceinline__ float mag(uint32_t v, uint32_t magic) {
 // One 32-bit word of nibbles (pair units U0..U0+3, one per byte) times its
 // x pairs.  Bytes 0 and 1 decode in place (classes 2^0,2^4 and 2^8,2^12);
 // bytes 2 and 3 after a 16-bit shift, into the same classes.
-template <int E, int U0, bool FIRST>
+template <int E, int OFF0, int U0, bool FIRST>
 __device__ __forceinline__ void word_fma(uint32_t v, uint32_t codes, uint32_t base,
                                          uint32_t magic, const ZConst& k, float2& a0,
                                          float2& a1, float2& a2, float2& a3) {
@@ -196,10 +210,10 @@ __device__ __forceinline__ void word_fma(uint32_t v, uint32_t codes, uint32_t ba
   d2 = __fadd2_rn(d2, k.ca);
   d3 = __fadd2_rn(d3, k.cb);
   // code of unit U0+s sits at bits 4s of `codes`; table stride 128 B/entry
-  const float2 x0 = lds_pair<(U0 + 0) * E * 128>(((codes << 7) & 0x780u) | base);
-  const float2 x1 = lds_pair<(U0 + 1) * E * 128>(((codes << 3) & 0x780u) | base);
-  const float2 x2 = lds_pair<(U0 + 2) * E * 128>(((codes >> 1) & 0x780u) | base);
-  const float2 x3 = lds_pair<(U0 + 3) * E * 128>(((codes >> 5) & 0x780u) | base);
+  const float2 x0 = lds_pair<OFF0 + (U0 + 0) * E * 128>(((codes << 7) & 0x780u) | base);
+  const float2 x1 = lds_pair<OFF0 + (U0 + 1) * E * 128>(((codes << 3) & 0x780u) | base);
+  const float2 x2 = lds_pair<OFF0 + (U0 + 2) * E * 128>(((codes >> 1) & 0x780u) | base);
+  const float2 x3 = lds_pair<OFF0 + (U0 + 3) * E * 128>(((codes >> 5) & 0x780u) | base);
   if (FIRST) {
     a0 = __fmul2_rn(d0, x0);
     a1 = __fmul2_rn(d1, x1);
@@ -237,23 +251,23 @@ template <int N, bool G2>
 __device__ __forceinline__ float chunk_dot(const uint4& v, const uint2& ix,
                                            uint32_t sa, uint32_t sb, uint32_t base,
                                            uint32_t magic) {
-  constexpr int E = M1Cfg<N>::E;
+  constexpr int E = M1Cfg<N>::E, O = M1Cfg<N>::OFF0;
   float2 a0, a1, a2, a3;
   if (!G2) {
     const ZConst k = zconst(sz_zero(sa));
-    word_fma<E, 0, true>(v.x, ix.x, base, magic, k, a0, a1, a2, a3);
-    word_fma<E, 4, false>(v.y, ix.x >> 16, base, magic, k, a0, a1, a2, a3);
-    word_fma<E, 8, false>(v.z, ix.y, base, magic, k, a0, a1, a2, a3);
-    word_fma<E, 12, false>(v.w, ix.y >> 16, base, magic, k, a0, a1, a2, a3);
+    word_fma<E, O, 0, true>(v.x, ix.x, base, magic, k, a0, a1, a2, a3);
+    word_fma<E, O, 4, false>(v.y, ix.x >> 16, base, magic, k, a0, a1, a2, a3);
+    word_fma<E, O, 8, false>(v.z, ix.y, base, magic, k, a0, a1, a2, a3);
+    word_fma<E, O, 12, false>(v.w, ix.y >> 16, base, magic, k, a0, a1, a2, a3);
     return sz_scale(sa) * fold(a0, a1, a2, a3);
   } else {
     const ZConst ka = zconst(sz_zero(sa));
-    word_fma<E, 0, true>(v.x, ix.x, base, magic, ka, a0, a1, a2, a3);
-    word_fma<E, 4, false>(v.y, ix.x >> 16, base, magic, ka, a0, a1, a2, a3);
+    word_fma<E, O, 0, true>(v.x, ix.x, base, magic, ka, a0, a1, a2, a3);
+    word_fma<E, O, 4, false>(v.y, ix.x >> 16, base, magic, ka, a0, a1, a2, a3);
     const float ya = sz_scale(sa) * fold(a0, a1, a2, a3);
     const ZConst kb = zconst(sz_zero(sb));
-    word_fma<E, 8, true>(v.z, ix.y, base, magic, kb, a0, a1, a2, a3);
-    word_fma<E, 12, false>(v.w, ix.y >> 16, base, magic, kb, a0, a1, a2, a3);
+    word_fma<E, O, 8, true>(v.z, ix.y, base, magic, kb, a0, a1, a2, a3);
+    word_fma<E, O, 12, false>(v.w, ix.y >> 16, base, magic, kb, a0, a1, a2, a3);
     return fmaf(sz_scale(sb), fold(a0, a1, a2, a3), ya);
   }
 }
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int S = p.cpl * kUnitsPerChunk * C::E;     // table slots per half-warp
+  const int S = p.cpl * C::SLOTS;                  // table slots per half-warp
   const int tab_bytes = 2 * S * 128;
   // The table starts on a 2 KB boundary so that bits 7..10 of every slot
   // address come from the code alone (the lookups OR the code in).
@@ -385,7 +399,7 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   const uint32_t ring_s = smem_s + (uint32_t)(tab_bytes + xs_bytes + part_bytes);
   const uint32_t my_ring = ring_s + (uint32_t)(warp * kS * kStage);
   const uint32_t lane_base = smem_s + (uint32_t)((lane >> 4) * S) * 128u + (lane & 15) * 8u;
-  constexpr uint32_t kChunkSlotBytes = kUnitsPerChunk * C::E * 128;
+  constexpr uint32_t kChunkSlotBytes = C::SLOTS * 128;   // a multiple of 2 KB
   uint32_t magic = 0x4B000000u;  // exponent of 2^23, kept in a register
   asm volatile("" : "+r"(magic));
 
@@ -397,8 +411,11 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   // the previous kernel); one commit group per item, empty past the end
   // The ring starts zeroed: a lane past a ragged slice reads a stage it did
   // not fill, and must find codes in range there (its table slots are zero).
-  for (int b = 16 * lane; b < kS * kStage; b += 16 * 32)
-    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(my_ring + b), "r"(0u) : "memory");
+  // (2:4: position nibbles 4 = (0, 1), the smallest code the table holds)
+  for (int b = 16 * lane; b < kS * kStage; b += 16 * 32) {
+    const uint32_t f = N == 2 && (b % kStage) >= kIdxOff && (b % kStage) < kSzOff ? 0x44444444u : 0u;
+    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(my_ring + b), "r"(f) : "memory");
+  }
   __syncwarp();
   // this lane's regions of ring stage 0 (nibbles; codes and scale/zero)
   const uint32_t ring16 = my_ring + 16 * lane, ring8 = my_ring + 8 * lane;
@@ -464,13 +481,16 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
 #pragma unroll
           for (int q = 0; q < C::UC; ++q) xv[q] = 0.0f;
         }
-        const uint32_t a = colbase + (uint32_t)(u_it * C::E) * 128u;
+        const uint32_t a = colbase + (uint32_t)(i * C::SLOTS + u * C::E) * 128u;
+        if constexpr (N == 2) {
 #pragma unroll
-        for (int e = 0; e < C::E; ++e) {
-          if (N == 2)
-            sts_pair(a + e * 128, xv[pair24_a(e)], xv[pair24_b(e)]);
-          else
-            sts_pair(a + e * 128, xv[e & 3], xv[4 + (e >> 2)]);
+          for (int e = 0; e < 6; ++e) {
+            const int nib = quad24_nibble(e);
+            sts_pair(a + (nib - 4) * 128, xv[nib & 3], xv[nib >> 2]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < C::E; ++e) sts_pair(a + e * 128, xv[e & 3], xv[4 + (e >> 2)]);
         }
       }
     }

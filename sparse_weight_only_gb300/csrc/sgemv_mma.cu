@@ -15,9 +15,9 @@
 //    both halves, one LOP3 keeps q_a in the low half's mantissa and q_b in
 //    the high half's (exponent patterns for 1024 and 64), one HSUB2 takes
 //    (1024 + z, 64 + z) off.  (q - z) is an integer in [-15, 15], exact.
-//  * metadata: the stored six-way pair codes become (a | b << 2) nibbles
-//    through a PRMT lookup table; thread (g, t in {0,1}) supplies quads
-//    4t..4t+3 of rows g (low half) and g + 8 (high half).
+//  * metadata: the stored position nibbles (a | b << 2) are the MMA's own
+//    format; thread (g, t in {0,1}) supplies quads 4t..4t+3 of rows g (low
+//    half) and g + 8 (high half), one PRMT of the two rows' code words.
 //  * B (32 x 8): x rows staged in shared memory (padded rows, so ldmatrix
 //    reads are conflict-free), one ldmatrix.x4 per n-tile and k-tile.
 //  * weights: the CTA's 128 rows x K sub-slice (codes, positions and the
@@ -61,17 +61,6 @@ struct MmaParams {
   int sub_chunks;     // chunks of weights and x staged at a time
   int sub_groups;     // scale/zero words per row staged per sub-slice (bound)
 };
-
-// code (0..5) -> (a | b << 2): (0,1)=4 (0,2)=8 (0,3)=12 (1,2)=9 (1,3)=13 (2,3)=14
-constexpr uint32_t kMetaLo = 0x090C0804u;
-constexpr uint32_t kMetaHi = 0x00000E0Du;
-
-// Four stored codes (a 16-bit field) -> four metadata nibbles (16 bits).
-__device__ __forceinline__ uint32_t meta16(uint32_t codes) {
-  uint32_t r = __byte_perm(kMetaLo, kMetaHi, codes & 0xFFFFu);
-  r |= r >> 4;
-  return __byte_perm(r, 0u, 0x4420u);
-}
 
 // half2 (q_a - z, q_b - z) of the quad whose byte is byte `t` of `w`.
 __device__ __forceinline__ uint32_t quad_h2(uint32_t w, uint32_t sel, uint32_t zc) {
@@ -158,6 +147,26 @@ struct WGeom {
   }
 };
 
+// (row, column) of a thread's pieces in an R x n block walked in steps of
+// the CTA size: one division at the start, then carries.
+struct Walk2D {
+  int r, c, dr, dc, n;
+  __device__ __forceinline__ Walk2D(int n_) : n(n_) {
+    r = (int)threadIdx.x / n;
+    c = (int)threadIdx.x - r * n;
+    dr = (kW * 32) / n;
+    dc = (kW * 32) - dr * n;
+  }
+  __device__ __forceinline__ void step() {
+    c += dc;
+    r += dr;
+    if (c >= n) {
+      c -= n;
+      ++r;
+    }
+  }
+};
+
 // Copies the weight block of rows [row0, row0 + 128) x chunks [cs, ce) and
 // the scale/zero words of groups [g0, g1] into a buffer; rows past the
 // matrix are skipped (their values are replaced when read).
@@ -165,17 +174,14 @@ __device__ __forceinline__ void stage_weights(const MmaParams& p, const WGeom& W
                                               int row0, int cs, int ce, int g0, int g1) {
   const int nc = ce - cs, ng = g1 - g0 + 1;
   const int nrow = min(kRowsCta, p.rows - row0);
-  for (int i = threadIdx.x; i < nrow * nc; i += kW * 32) {
-    const int r = i / nc, cc = i - r * nc;
-    const size_t src = (size_t)(row0 + r) * p.cstride + cs + cc;
-    cp_async<16>(buf + W.vals_off + r * W.vst + cc * 16, p.vals + src);
-    cp_async<8>(buf + W.idx_off + r * W.ist + cc * 8, p.idx + src);
+  for (Walk2D w(nc); w.r < nrow; w.step()) {
+    const size_t src = (size_t)(row0 + w.r) * p.cstride + cs + w.c;
+    cp_async<16>(buf + W.vals_off + w.r * W.vst + w.c * 16, p.vals + src);
+    cp_async<8>(buf + W.idx_off + w.r * W.ist + w.c * 8, p.idx + src);
   }
-  for (int i = threadIdx.x; i < nrow * ng; i += kW * 32) {
-    const int r = i / ng, gg = i - r * ng;
-    cp_async<4>(buf + W.sz_off + r * W.sst + gg * 4,
-                p.sz + (size_t)(row0 + r) * p.gstride + g0 + gg);
-  }
+  for (Walk2D w(ng); w.r < nrow; w.step())
+    cp_async<4>(buf + W.sz_off + w.r * W.sst + w.c * 4,
+                p.sz + (size_t)(row0 + w.r) * p.gstride + g0 + w.c);
 }
 
 template <int NT>
@@ -214,6 +220,8 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
 
   // selectors copying byte t (or t + 4 of the word pair) into bytes 0 and 2
   const uint32_t sel = 0x4040u | (uint32_t)t | ((uint32_t)t << 8);
+  // ... and the 16-bit metadata field of thread t from rows g, g + 8
+  const uint32_t msel = (t & 1) ? 0x7632u : 0x5410u;
   float s_g = 0.0f, s_g8 = 0.0f;
   uint32_t zc_g = 0, zc_g8 = 0;
   int cur_group = -1;
@@ -243,14 +251,11 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
     cp_commit();
     {
       // stage x[:, 64 cs .. 64 ce) (zero for padded rows)
-      const int ncol = (ce - cs) * 64;
-      const int pieces = mp * (ncol / 8);
-      for (int i = threadIdx.x; i < pieces; i += kW * 32) {
-        const int row = i / (ncol / 8), c8 = i % (ncol / 8);
+      for (Walk2D w((ce - cs) * 8); w.r < mp; w.step()) {
         uint4 q = make_uint4(0, 0, 0, 0);
-        if (row < p.m)
-          q = *reinterpret_cast<const uint4*>(p.x + (size_t)row * p.cols + cs * 64 + c8 * 8);
-        *reinterpret_cast<uint4*>(xs + row * xs_stride + c8 * 8) = q;
+        if (w.r < p.m)
+          q = *reinterpret_cast<const uint4*>(p.x + (size_t)w.r * p.cols + cs * 64 + w.c * 8);
+        *reinterpret_cast<uint4*>(xs + w.r * xs_stride + w.c * 8) = q;
       }
     }
     cp_wait<1>();     // this thread's copies of sub-slice sidx landed
@@ -293,10 +298,9 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
         const uint32_t a1 = quad_h2(wlo_g8, sel, zc_g8);  // row g+8, quad t
         const uint32_t a2 = quad_h2(whi_g, sel, zc_g);    // row g,   quad t+4
         const uint32_t a3 = quad_h2(whi_g8, sel, zc_g8);  // row g+8, quad t+4
-        // metadata (threads t = 0, 1): quads 4t..4t+3 of rows g and g+8
-        const uint32_t cw_g = kt ? i_g.y : i_g.x, cw_g8 = kt ? i_g8.y : i_g8.x;
-        const uint32_t sh = (t & 1) * 16;
-        const uint32_t meta = meta16(cw_g >> sh) | (meta16(cw_g8 >> sh) << 16);
+        // metadata (threads t = 0, 1): the stored position nibbles of quads
+        // 4t..4t+3 of this k-tile, row g in the low half, row g+8 in the high
+        const uint32_t meta = __byte_perm(kt ? i_g.y : i_g.x, kt ? i_g8.y : i_g8.x, msel);
         const uint32_t kofs = (uint32_t)((cc * 64 + kt * 32) * 2);
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
