@@ -47,6 +47,9 @@ constexpr int kRowsCta = 16 * kW;     // weight rows per CTA
 #endif
 constexpr int kMaxSplit = SGEMV_MMA_MAXSPLIT;  // CTAs per cluster (portable limit 8)
 constexpr size_t kSmemPerCta = 113 * 1024;  // two CTAs per SM
+#ifndef SGEMV_MMA_PDL
+#define SGEMV_MMA_PDL 1
+#endif
 
 struct MmaParams {
   const uint4* vals;
@@ -236,6 +239,9 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
                   (ce * 64 - 1) >> p.gshift);
   }
   cp_commit();
+  // x may be written by the previous kernel: wait for it only now
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
 
   for (int sidx = 0; sidx < nsub; ++sidx) {
     const int cs = c_begin + sidx * p.sub_chunks;
@@ -419,13 +425,15 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
   cfg.blockDim = dim3(kW * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = nsplit;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = SGEMV_MMA_PDL ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_mma24<NT>, p);
 }
 
