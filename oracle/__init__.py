@@ -77,6 +77,10 @@ def _load():
         lib.orc_decode.restype = None
         lib.orc_pack.argtypes = [P, I64, I64, I, I, P, P, P, P]
         lib.orc_pack.restype = I
+        lib.orc_prune_scored.argtypes = [P, P, P, I64, I64, I, P]
+        lib.orc_prune_scored.restype = I
+        lib.orc_pack_scored.argtypes = [P, P, P, I64, I64, I, I, P, P, P, P]
+        lib.orc_pack_scored.restype = I
         lib.orc_dequant_rows.argtypes = [P, P, P, P, I64, I, I, I64, I64, P]
         lib.orc_dequant_rows.restype = None
         lib.orc_matvec.argtypes = [P, P, P, P, I64, I, I, P, I, P, I64, P]
@@ -133,6 +137,20 @@ def prune(W: np.ndarray, n_keep: int) -> np.ndarray:
     rc = _load().orc_prune(_ptr(W), rows, cols, n_keep, _ptr(pos))
     if rc:
         raise OracleError(rc, "prune")
+    return pos
+
+
+def prune_scored(W: np.ndarray, xnorm: np.ndarray, grad, n_keep: int) -> np.ndarray:
+    """Eq. 3 pruning: keep per quad the N largest |w|*xnorm + |w|*|grad|."""
+    W = _c(W, np.float32)
+    rows, cols = W.shape
+    xn = _c(xnorm, np.float32)
+    g = None if grad is None else _c(grad, np.float32)
+    pos = np.zeros((rows, cols // 4, n_keep), dtype=np.uint8)
+    rc = _load().orc_prune_scored(_ptr(W), _ptr(xn), None if g is None else _ptr(g),
+                                  rows, cols, n_keep, _ptr(pos))
+    if rc:
+        raise OracleError(rc, "prune_scored")
     return pos
 
 
@@ -226,3 +244,24 @@ def matvec(p: Packed, x_f16: np.ndarray, rows=None) -> np.ndarray:
                        p.cols, p.n_keep, p.group, _ptr(x), m, _ptr(rows),
                        rows.size, _ptr(y))
     return np.ascontiguousarray(y.T)
+
+
+def pack_scored(W: np.ndarray, xnorm: np.ndarray, grad, n_keep: int,
+                group: int) -> Packed:
+    """Eq. 3 pruning, then the same quantisation and encoding as pack()."""
+    W = _c(W, np.float32)
+    rows, cols = W.shape
+    xn = _c(xnorm, np.float32)
+    g = None if grad is None else _c(grad, np.float32)
+    vb, ib = row_bytes(cols, n_keep)
+    ng = cols // group if group else 0
+    vals = np.zeros((rows, vb), dtype=np.uint8)
+    idx = np.zeros((rows, ib), dtype=np.uint8)
+    scale = np.zeros((rows, ng), dtype=np.uint16)
+    zero = np.zeros((rows, ng), dtype=np.uint16)
+    rc = _load().orc_pack_scored(_ptr(W), _ptr(xn), None if g is None else _ptr(g),
+                                 rows, cols, n_keep, group, _ptr(vals), _ptr(idx),
+                                 _ptr(scale), _ptr(zero))
+    if rc:
+        raise OracleError(rc, "pack_scored")
+    return Packed(rows, cols, n_keep, group, vals, idx, scale, zero)

@@ -18,6 +18,9 @@
  *      [0, 15]; the range [lo, hi] always includes 0; s is (hi - lo) / 15
  *      rounded to binary16; rounding is round-half-to-even throughout.
  *   R3 layout: the canonical 2bit-CSR bytes described in the header.
+ *   R11 importance score: Eq. 3 evaluated in binary32 as written (see
+ *      orc_prune_scored); magnitude pruning (R1) is its case of equal norms
+ *      and zero gradient.
  */
 #include "sgemv_oracle.h"
 
@@ -224,6 +227,81 @@ void orc_decode(const uint8_t* vals, const uint8_t* idx, int64_t rows,
       pos[r * P + j] = (idx[r * ib + j / 4] >> (2 * (j % 4))) & 0x3;
     }
   }
+}
+
+/* O1 with the paper's importance score (section 3.2, Eq. 3):
+ *   score_ij = |W_ij| * ||X_j||_2 + |W_ij| * |dE/dW_ij|,
+ * with the activation norms of the input columns and the loss gradient
+ * supplied by the caller (grad NULL: zero gradient).  Reading R11: the
+ * score is evaluated in binary32 exactly as written -- t1 = |w| * xn,
+ * t2 = |w| * |g|, score = t1 + t2, each one rounding -- and each quad keeps
+ * the N largest scores, the lower column first on equal scores, like R1.
+ * NaN/Inf in W, xnorm or grad -> ORC_ERR_NONFINITE; a negative norm ->
+ * ORC_ERR_ARG. */
+int orc_prune_scored(const float* W, const float* xnorm, const float* grad,
+                     int64_t rows, int64_t cols, int n_keep, uint8_t* pos) {
+  if (!shape_ok(rows, cols, n_keep) || !xnorm) return ORC_ERR_ARG;
+  for (int64_t c = 0; c < cols; ++c) {
+    if (!isfinite(xnorm[c])) return ORC_ERR_NONFINITE;
+    if (xnorm[c] < 0.0f) return ORC_ERR_ARG;
+  }
+  int64_t quads = cols / 4;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t t = 0; t < quads; ++t) {
+      float sc[4];
+      for (int i = 0; i < 4; ++i) {
+        int64_t c = 4 * t + i;
+        float w = W[r * cols + c];
+        float g = grad ? grad[r * cols + c] : 0.0f;
+        if (!isfinite(w) || !isfinite(g)) return ORC_ERR_NONFINITE;
+        float aw = fabsf(w);
+        float t1 = aw * xnorm[c];
+        float t2 = aw * fabsf(g);
+        sc[i] = t1 + t2;
+      }
+      uint8_t* out = pos + (r * quads + t) * n_keep;
+      int k = 0;
+      for (int i = 0; i < 4; ++i) {
+        int ahead = 0;
+        for (int j = 0; j < 4; ++j) {
+          if (j == i) continue;
+          if (sc[j] > sc[i] || (sc[j] == sc[i] && j < i)) ahead++;
+        }
+        if (ahead < n_keep) out[k++] = (uint8_t)i;
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+/* O1 (by `pos` already chosen) + O2 + O3. */
+static int pack_from_pos(const float* W, uint8_t* pos, int64_t rows,
+                         int64_t cols, int n_keep, int group, uint8_t* vals,
+                         uint8_t* idx, uint16_t* scale, uint16_t* zero) {
+  int64_t P = cols / 4 * n_keep;
+  size_t n = (size_t)(rows * P);
+  uint8_t* q = (uint8_t*)malloc(n ? n : 1);
+  if (!q) return ORC_ERR_ARG;
+  int rc = orc_quantize(W, pos, rows, cols, n_keep, group, q, scale, zero);
+  if (rc == ORC_OK) orc_encode(pos, q, rows, cols, n_keep, vals, idx);
+  free(q);
+  return rc;
+}
+
+int orc_pack_scored(const float* W, const float* xnorm, const float* grad,
+                    int64_t rows, int64_t cols, int n_keep, int group,
+                    uint8_t* vals, uint8_t* idx, uint16_t* scale,
+                    uint16_t* zero) {
+  if (!shape_ok(rows, cols, n_keep)) return ORC_ERR_ARG;
+  int64_t P = cols / 4 * n_keep;
+  size_t n = (size_t)(rows * P);
+  uint8_t* pos = (uint8_t*)malloc(n ? n : 1);
+  if (!pos) return ORC_ERR_ARG;
+  int rc = orc_prune_scored(W, xnorm, grad, rows, cols, n_keep, pos);
+  if (rc == ORC_OK)
+    rc = pack_from_pos(W, pos, rows, cols, n_keep, group, vals, idx, scale, zero);
+  free(pos);
+  return rc;
 }
 
 int orc_pack(const float* W, int64_t rows, int64_t cols, int n_keep,

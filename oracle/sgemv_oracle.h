@@ -77,6 +77,20 @@ void orc_encode(const uint8_t* pos, const uint8_t* q, int64_t rows,
 void orc_decode(const uint8_t* vals, const uint8_t* idx, int64_t rows,
                 int64_t cols, int n_keep, uint8_t* pos, uint8_t* q);
 
+/* O1 by the paper's Eq. 3 importance score
+ *   score = |W_ij| * xnorm[j] + |W_ij| * |grad_ij|
+ * in binary32 as written (two products, one sum, each rounded once), the N
+ * largest per quad, ties to the lower column.  xnorm: cols finite values
+ * >= 0; grad: rows x cols or NULL (zero gradient). */
+int orc_prune_scored(const float* W, const float* xnorm, const float* grad,
+                     int64_t rows, int64_t cols, int n_keep, uint8_t* pos);
+
+/* orc_prune_scored + O2 + O3. */
+int orc_pack_scored(const float* W, const float* xnorm, const float* grad,
+                    int64_t rows, int64_t cols, int n_keep, int group,
+                    uint8_t* vals, uint8_t* idx, uint16_t* scale,
+                    uint16_t* zero);
+
 /* O1 + O2 + O3 in one call, scratch allocated internally. */
 int orc_pack(const float* W, int64_t rows, int64_t cols, int n_keep,
              int group, uint8_t* vals, uint8_t* idx, uint16_t* scale,

@@ -153,6 +153,102 @@ def test_prune_rejects_nonfinite(orc):
 
 
 # ---------------------------------------------------------------------------
+# Eq. 3 pruning with caller-supplied input-channel norms and gradient.
+# ---------------------------------------------------------------------------
+
+def _eq3_brute(W, xnorm, grad, n_keep):
+    """Independent restatement: binary32 products and sum via numpy float32
+    scalars, then the top-N of each quad by (larger score, lower column)."""
+    rows, cols = W.shape
+    out = np.zeros((rows, cols // 4, n_keep), np.uint8)
+    for r in range(rows):
+        for t in range(cols // 4):
+            sc = []
+            for i in range(4):
+                c = 4 * t + i
+                aw = np.float32(abs(W[r, c]))
+                g = np.float32(0.0) if grad is None else np.float32(abs(grad[r, c]))
+                sc.append((np.float32(aw * np.float32(xnorm[c])) + np.float32(aw * g), i))
+            kept = sorted(i for _, i in sorted(sc, key=lambda e: (-float(e[0]), e[1]))[:n_keep])
+            out[r, t] = kept
+    return out
+
+
+@pytest.mark.parametrize("n_keep", [1, 2])
+def test_prune_scored_brute_force(orc, n_keep):
+    rng = np.random.default_rng(11 + n_keep)
+    W = rng.normal(0, 0.05, (6, 64)).astype(np.float32)
+    W[0, :8] = [0.1, -0.1, 0.1, 0.0, -0.0, 0.0, 0.2, -0.2]   # ties in |w|
+    xnorm = rng.uniform(0, 4, 64).astype(np.float32)
+    xnorm[8:12] = 0.0                                           # all-zero scores
+    grad = rng.normal(0, 0.5, (6, 64)).astype(np.float32)
+    for g in (grad, None):
+        assert np.array_equal(orc.prune_scored(W, xnorm, g, n_keep),
+                              _eq3_brute(W, xnorm, g, n_keep))
+
+
+def test_prune_scored_hand_cases(orc):
+    # row 0: the gradient term makes the smallest |w| the largest score
+    #   scores (1 + 10, 2, 3, 4) -> keep (0, 3); N = 1 keeps 0
+    # row 0, quad 1: |w| (4, 3, 2, 1) with norms (0, 0, 1, 10): scores
+    #   (0, 0, 2, 10) -> keep (2, 3); N = 1 keeps 3
+    W = np.array([[1, 2, 3, 4, 4, 3, 2, 1]], np.float32)
+    xnorm = np.array([1, 1, 1, 1, 0, 0, 1, 10], np.float32)
+    grad = np.zeros_like(W)
+    grad[0, 0] = -10.0
+    assert orc.prune_scored(W, xnorm, grad, 2).tolist() == [[[0, 3], [2, 3]]]
+    assert orc.prune_scored(W, xnorm, grad, 1).tolist() == [[[0], [3]]]
+    # equal scores from different (w, norm) pairs: ties go to the lower column
+    W2 = np.array([[2, 1, 4, 1]], np.float32)
+    xn2 = np.array([1, 2, 0.5, 1], np.float32)
+    assert orc.prune_scored(W2, xn2, None, 2).tolist() == [[[0, 1]]]
+
+
+@pytest.mark.parametrize("c", [1.0, 0.25, 8.0])
+def test_prune_scored_is_magnitude_at_power_of_two_norms(orc, c):
+    """A constant power-of-two norm scales every score exactly, so the
+    selection is the magnitude pruning's, bit for bit."""
+    W = synth.weight_outliers(7, 16, 256)
+    xnorm = np.full(256, c, np.float32)
+    for n_keep in (1, 2):
+        assert np.array_equal(orc.prune_scored(W, xnorm, None, n_keep), orc.prune(W, n_keep))
+        assert np.array_equal(orc.prune_scored(W, xnorm, np.zeros_like(W), n_keep),
+                              orc.prune(W, n_keep))
+
+
+def test_prune_scored_rejects_bad_inputs(orc):
+    W = np.ones((2, 8), np.float32)
+    xn = np.ones(8, np.float32)
+    g = np.zeros((2, 8), np.float32)
+    for arr, i, bad, code in ((xn, 3, np.nan, orc.ORC_ERR_NONFINITE),
+                              (xn, 3, -1.0, orc.ORC_ERR_ARG),
+                              (g, (1, 6), np.inf, orc.ORC_ERR_NONFINITE),
+                              (W, (0, 2), np.nan, orc.ORC_ERR_NONFINITE)):
+        a = arr.copy()
+        a[i] = bad
+        args = {"W": W, "xn": xn, "g": g}
+        args[{id(xn): "xn", id(g): "g", id(W): "W"}[id(arr)]] = a
+        with pytest.raises(orc.OracleError) as e:
+            orc.prune_scored(args["W"], args["xn"], args["g"], 2)
+        assert e.value.code == code
+
+
+def test_pack_scored_composes_the_steps(orc):
+    W = synth.weight_normal(3, 8, 256, 0.02)
+    rng = np.random.default_rng(5)
+    xn = rng.uniform(0.5, 2, 256).astype(np.float32)
+    g = rng.normal(0, 1, (8, 256)).astype(np.float32)
+    p = orc.pack_scored(W, xn, g, 2, 64)
+    pos = orc.prune_scored(W, xn, g, 2)
+    q, sc, z = orc.quantize(W, pos, 2, 64)
+    vals, idx = orc.encode(pos, q, 8, 256, 2)
+    assert np.array_equal(p.vals, vals) and np.array_equal(p.idx, idx)
+    assert np.array_equal(p.scale, sc) and np.array_equal(p.zero, z)
+    # and the scores changed the selection somewhere (the test is not vacuous)
+    assert not np.array_equal(pos, orc.prune(W, 2))
+
+
+# ---------------------------------------------------------------------------
 # Hand-derived tiny cases: prune + quantise + encode + dequant + matvec.
 # ---------------------------------------------------------------------------
 
