@@ -101,6 +101,24 @@ int sgemv_pack(sgemv_t h, const float* w_host);
 int sgemv_pack_device(sgemv_t h, const float* w_dev, void* stream);
 
 /*
+ * As sgemv_pack, but each quad keeps the N weights of largest importance
+ * score, the pruning criterion of the paper (section 3.2, "Sparsification",
+ * Eq. 3):
+ *   score_ij = |W_ij| * xnorm[j] + |W_ij| * |grad_ij|,
+ * evaluated in binary32 as written (two products and one sum, each rounded
+ * to nearest once), ties to the lower column.  Quantisation is unchanged.
+ *   xnorm_host : cols values, the L2 norm of input channel j over the
+ *                caller's calibration activations; finite and >= 0
+ *                (SGEMV_ERR_NONFINITE / SGEMV_ERR_ARG otherwise);
+ *   grad_host  : rows x cols row-major, the loss gradient dE/dW, or NULL for
+ *                a zero gradient; NaN/Inf -> SGEMV_ERR_NONFINITE.
+ * All three host arrays are read only.  With every norm equal to a power of
+ * two and no gradient the result equals sgemv_pack's.  Synchronous.
+ */
+int sgemv_pack_scored(sgemv_t h, const float* w_host, const float* xnorm_host,
+                      const float* grad_host);
+
+/*
  * Load canonical 2bit-CSR bytes (host memory, layout above; the byte counts
  * are those reported by sgemv_sizes).  For N = 2 the two positions of each
  * quad must ascend strictly (SGEMV_ERR_ARG otherwise).  Synchronous.

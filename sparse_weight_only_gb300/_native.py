@@ -34,6 +34,7 @@ SIGNATURES = {
     "sgemv_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _I, _I]),
     "sgemv_pack": (_I, [_P, _P]),
     "sgemv_pack_device": (_I, [_P, _P, _P]),
+    "sgemv_pack_scored": (_I, [_P, _P, _P, _P]),
     "sgemv_import": (_I, [_P, _P, _P, _P, _P]),
     "sgemv_export": (_I, [_P, _P, _P, _P, _P]),
     "sgemv_run": (_I, [_P, _P, _P, _I, _P]),
@@ -147,6 +148,24 @@ class SparseGemv:
         if w.shape != (self.rows, self.cols):
             raise ValueError(f"weight shape {w.shape} != {(self.rows, self.cols)}")
         _check(load().sgemv_pack(self._h, w.ctypes.data), "sgemv_pack")
+
+    def pack_scored(self, w: np.ndarray, xnorm: np.ndarray, grad=None) -> None:
+        """Eq. 3 importance pruning: |w| * xnorm[col] + |w| * |grad| per
+        weight (grad None: zero gradient), then the usual quantisation."""
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        if w.shape != (self.rows, self.cols):
+            raise ValueError(f"weight shape {w.shape} != {(self.rows, self.cols)}")
+        xn = np.ascontiguousarray(xnorm, dtype=np.float32)
+        if xn.shape != (self.cols,):
+            raise ValueError(f"xnorm shape {xn.shape} != {(self.cols,)}")
+        g = None
+        if grad is not None:
+            g = np.ascontiguousarray(grad, dtype=np.float32)
+            if g.shape != w.shape:
+                raise ValueError(f"grad shape {g.shape} != {w.shape}")
+        _check(load().sgemv_pack_scored(self._h, w.ctypes.data, xn.ctypes.data,
+                                        None if g is None else g.ctypes.data),
+               "sgemv_pack_scored")
 
     def pack_device(self, w, stream=None) -> None:
         """w: a torch float32 CUDA tensor of shape (rows, cols)."""

@@ -2,10 +2,12 @@
 // include/sgemv.h): argument checks, handle and device-buffer management,
 // host<->device transfers, and kernel dispatch.  No arithmetic of the
 // method happens here; every step of pack and run executes in the CUDA
-// kernels of sgemv_format.cu, sgemv_generic.cu and sgemv_m1.cu.
+// kernels of sgemv_format.cu, sgemv_generic.cu, sgemv_m1.cu and sgemv_mma.cu.
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
+
+#include <cmath>
 
 #include "sgemv_internal.cuh"
 
@@ -117,7 +119,8 @@ void free_ctx(sgemv_t h) {
   delete h;
 }
 
-int pack_on_device(sgemv_t h, const float* w_dev, cudaStream_t s) {
+int pack_on_device(sgemv_t h, const float* w_dev, cudaStream_t s, const float* xnorm_dev = nullptr,
+                   const float* grad_dev = nullptr) {
   const sgemv::Layout& L = h->L;
   h->ready = false;
   CUDA_TRY(cudaMemsetAsync(h->d_err, 0, sizeof(int), s), "clear error word");
@@ -127,7 +130,8 @@ int pack_on_device(sgemv_t h, const float* w_dev, cudaStream_t s) {
     CUDA_TRY(cudaMemsetAsync(h->d_idx, 0, idx_dev_bytes(L), s), "memset idx");
   if (sz_dev_bytes(L))
     CUDA_TRY(cudaMemsetAsync(h->d_sz, 0, sz_dev_bytes(L), s), "memset scale/zero");
-  CUDA_TRY(sgemv::launch_pack(L, w_dev, h->d_vals, h->d_idx, h->d_sz, h->d_err, s),
+  CUDA_TRY(sgemv::launch_pack(L, w_dev, xnorm_dev, grad_dev, h->d_vals, h->d_idx, h->d_sz,
+                              h->d_err, s),
            "pack kernel");
   CUDA_TRY(cudaStreamSynchronize(s), "pack");
   int word = 0;
@@ -225,6 +229,40 @@ int sgemv_pack(sgemv_t h, const float* w_host) {
                              h->stream),
              "copy weight to device");
   return pack_on_device(h, static_cast<const float*>(w.p), h->stream);
+}
+
+int sgemv_pack_scored(sgemv_t h, const float* w_host, const float* xnorm_host,
+                      const float* grad_host) {
+  if (int rc = check_handle(h)) return rc;
+  const sgemv::Layout& L = h->L;
+  const size_t n = (size_t)L.rows * L.cols;
+  if (n && !w_host) return fail(SGEMV_ERR_ARG, "w_host is NULL");
+  if (L.cols && !xnorm_host) return fail(SGEMV_ERR_ARG, "xnorm_host is NULL");
+  for (int c = 0; c < L.cols; ++c) {
+    if (!std::isfinite(xnorm_host[c]))
+      return fail(SGEMV_ERR_NONFINITE, "xnorm[%d] is not finite", c);
+    if (xnorm_host[c] < 0.0f) return fail(SGEMV_ERR_ARG, "xnorm[%d] is negative", c);
+  }
+  DeviceGuard g(h->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  DevBuf w, xn, gr;
+  CUDA_TRY(w.alloc(n * sizeof(float)), "cudaMalloc dense weight");
+  CUDA_TRY(xn.alloc((size_t)L.cols * sizeof(float)), "cudaMalloc norms");
+  if (grad_host) CUDA_TRY(gr.alloc(n * sizeof(float)), "cudaMalloc gradient");
+  if (n) {
+    CUDA_TRY(cudaMemcpyAsync(w.p, w_host, n * sizeof(float), cudaMemcpyHostToDevice, h->stream),
+             "copy weight to device");
+    if (grad_host)
+      CUDA_TRY(cudaMemcpyAsync(gr.p, grad_host, n * sizeof(float), cudaMemcpyHostToDevice,
+                               h->stream),
+               "copy gradient to device");
+  }
+  if (L.cols)
+    CUDA_TRY(cudaMemcpyAsync(xn.p, xnorm_host, (size_t)L.cols * sizeof(float),
+                             cudaMemcpyHostToDevice, h->stream),
+             "copy norms to device");
+  return pack_on_device(h, static_cast<const float*>(w.p), h->stream,
+                        static_cast<const float*>(xn.p), static_cast<const float*>(gr.p));
 }
 
 int sgemv_pack_device(sgemv_t h, const float* w_dev, void* stream) {

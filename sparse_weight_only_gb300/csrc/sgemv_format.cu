@@ -21,13 +21,11 @@ __device__ __forceinline__ void set_err(int* err, int code) {
 }
 
 // Keep-set of one quad: element i is kept iff fewer than N elements precede
-// it in the order (larger |w| first, lower column first on ties).
+// it in the order (larger score first, lower column first on ties).  The
+// score is |w| (magnitude pruning) or the caller-weighted importance a[i].
 template <int N>
-__device__ __forceinline__ void prune_quad(const float w[4], int pos[N],
+__device__ __forceinline__ void prune_quad(const float w[4], const float a[4], int pos[N],
                                            float val[N]) {
-  float a[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) a[i] = fabsf(w[i]);
   int k = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -46,8 +44,13 @@ __device__ __forceinline__ void prune_quad(const float w[4], int pos[N],
 
 // One thread per (row, 16 dense columns).  Groups are 64..256 columns, so a
 // group is 4..16 consecutive threads of one warp, reduced by xor-shuffles.
+// With xnorm set, pruning ranks by the importance score of Eq. 3 (section
+// 3.2): |w| * xnorm[col] + |w| * |grad| (grad NULL: zero gradient), two
+// products and a sum each rounded once in binary32, as written.
 template <int N>
 __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict__ w,
+                                             const float* __restrict__ xnorm,
+                                             const float* __restrict__ grad,
                                              uint8_t* __restrict__ vals,
                                              uint8_t* __restrict__ idx,
                                              uint32_t* __restrict__ sz,
@@ -75,6 +78,35 @@ __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict_
   bool bad = false;
 #pragma unroll
   for (int i = 0; i < 16; ++i) bad |= !isfinite(wv[i]);
+  float sc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) sc[i] = fabsf(wv[i]);
+  if (xnorm && active) {
+    const float4* xs = reinterpret_cast<const float4*>(xnorm + 16 * k);
+    float gv[16];
+    if (grad) {
+      const float4* gs = reinterpret_cast<const float4*>(grad + r * L.cols + 16 * k);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 f = gs[i];
+        gv[4 * i] = f.x; gv[4 * i + 1] = f.y; gv[4 * i + 2] = f.z; gv[4 * i + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) gv[i] = 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 n = xs[i];
+      const float nv[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * i + e;
+        bad |= !isfinite(gv[j]);
+        sc[j] = __fadd_rn(__fmul_rn(sc[j], nv[e]), __fmul_rn(sc[j], fabsf(gv[j])));
+      }
+    }
+  }
   if (bad) set_err(err, kDevErrNonfinite);
 
   int pos[4][N];
@@ -82,7 +114,7 @@ __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict_
   float lo = 0.0f, hi = 0.0f;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    prune_quad<N>(&wv[4 * t], pos[t], val[t]);
+    prune_quad<N>(&wv[4 * t], &sc[4 * t], pos[t], val[t]);
 #pragma unroll
     for (int n = 0; n < N; ++n) {
       lo = fminf(lo, val[t][n]);
@@ -251,16 +283,16 @@ inline unsigned blocks_for(int64_t n, int threads) {
 
 }  // namespace
 
-cudaError_t launch_pack(const Layout& L, const float* w, uint4* vals, uint2* idx,
-                        uint32_t* sz, int* err, cudaStream_t s) {
+cudaError_t launch_pack(const Layout& L, const float* w, const float* xnorm, const float* grad,
+                        uint4* vals, uint2* idx, uint32_t* sz, int* err, cudaStream_t s) {
   const int64_t total = (int64_t)L.rows * (L.cols / 16);
   if (total == 0) return cudaSuccess;
   const unsigned nb = blocks_for(total, 256);
   if (L.n_keep == 2)
-    k_pack<2><<<nb, 256, 0, s>>>(L, w, reinterpret_cast<uint8_t*>(vals),
+    k_pack<2><<<nb, 256, 0, s>>>(L, w, xnorm, grad, reinterpret_cast<uint8_t*>(vals),
                                  reinterpret_cast<uint8_t*>(idx), sz, err);
   else
-    k_pack<1><<<nb, 256, 0, s>>>(L, w, reinterpret_cast<uint8_t*>(vals),
+    k_pack<1><<<nb, 256, 0, s>>>(L, w, xnorm, grad, reinterpret_cast<uint8_t*>(vals),
                                  reinterpret_cast<uint8_t*>(idx), sz, err);
   return cudaGetLastError();
 }

@@ -67,8 +67,10 @@ constexpr int kDevErrBadIndex = 3;
 constexpr int kDevErrTimeout = 4;
 
 // ---- format kernels (sgemv_format.cu) ----
-cudaError_t launch_pack(const Layout& L, const float* w, uint4* vals, uint2* idx,
-                        uint32_t* sz, int* err, cudaStream_t s);
+// xnorm (cols values) selects Eq. 3 importance pruning, with grad (rows x
+// cols) or a zero gradient when grad is NULL; xnorm NULL: magnitude pruning.
+cudaError_t launch_pack(const Layout& L, const float* w, const float* xnorm, const float* grad,
+                        uint4* vals, uint2* idx, uint32_t* sz, int* err, cudaStream_t s);
 cudaError_t launch_canon_to_device(const Layout& L, const uint8_t* cvals,
                                    const uint8_t* cidx, const uint16_t* scale,
                                    const uint16_t* zero, uint4* vals, uint2* idx,
