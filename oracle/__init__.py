@@ -81,6 +81,14 @@ def _load():
         lib.orc_prune_scored.restype = I
         lib.orc_pack_scored.argtypes = [P, P, P, I64, I64, I, I, P, P, P, P]
         lib.orc_pack_scored.restype = I
+        lib.orc_quantize_rowg.argtypes = [P, P, I64, I64, I, P, P, P, P]
+        lib.orc_quantize_rowg.restype = I
+        lib.orc_pack_rowg.argtypes = [P, I64, I64, I, P, P, P, P, P]
+        lib.orc_pack_rowg.restype = I
+        lib.orc_dequant_rows_rowg.argtypes = [P, P, P, P, I64, I, P, I64, I64, P]
+        lib.orc_dequant_rows_rowg.restype = None
+        lib.orc_matvec_rowg.argtypes = [P, P, P, P, I64, I64, I, P, P, I, P, I64, P]
+        lib.orc_matvec_rowg.restype = None
         lib.orc_dequant_rows.argtypes = [P, P, P, P, I64, I, I, I64, I64, P]
         lib.orc_dequant_rows.restype = None
         lib.orc_matvec.argtypes = [P, P, P, P, I64, I, I, P, I, P, I64, P]
@@ -194,11 +202,14 @@ def decode(vals: np.ndarray, idx: np.ndarray, rows: int, cols: int,
 
 
 class Packed:
-    """Canonical 2bit-CSR arrays of one weight matrix."""
+    """Canonical 2bit-CSR arrays of one weight matrix.  With per-row group
+    sizes, `row_group` holds them (int32, one per row), `group` is None and
+    scale/zero are flat: each row's cols/row_group[r] entries in row order."""
 
-    def __init__(self, rows, cols, n_keep, group, vals, idx, scale, zero):
+    def __init__(self, rows, cols, n_keep, group, vals, idx, scale, zero, row_group=None):
         self.rows, self.cols, self.n_keep, self.group = rows, cols, n_keep, group
         self.vals, self.idx, self.scale, self.zero = vals, idx, scale, zero
+        self.row_group = row_group
 
 
 def pack(W: np.ndarray, n_keep: int, group: int) -> Packed:
@@ -221,6 +232,11 @@ def dequant(p: Packed, row0: int = 0, nrows: int | None = None) -> np.ndarray:
     if nrows is None:
         nrows = p.rows - row0
     out = np.zeros((nrows, p.cols), dtype=np.float64)
+    if p.row_group is not None:
+        _load().orc_dequant_rows_rowg(_ptr(p.vals), _ptr(p.idx), _ptr(p.scale),
+                                      _ptr(p.zero), p.cols, p.n_keep,
+                                      _ptr(p.row_group), row0, nrows, _ptr(out))
+        return out
     _load().orc_dequant_rows(_ptr(p.vals), _ptr(p.idx), _ptr(p.scale),
                              _ptr(p.zero), p.cols, p.n_keep, p.group, row0,
                              nrows, _ptr(out))
@@ -240,6 +256,11 @@ def matvec(p: Packed, x_f16: np.ndarray, rows=None) -> np.ndarray:
         rows = np.arange(p.rows, dtype=np.int64)
     rows = _c(rows, np.int64)
     y = np.zeros((rows.size, m), dtype=np.float64)
+    if p.row_group is not None:
+        _load().orc_matvec_rowg(_ptr(p.vals), _ptr(p.idx), _ptr(p.scale), _ptr(p.zero),
+                                p.rows, p.cols, p.n_keep, _ptr(p.row_group), _ptr(x), m,
+                                _ptr(rows), rows.size, _ptr(y))
+        return np.ascontiguousarray(y.T)
     _load().orc_matvec(_ptr(p.vals), _ptr(p.idx), _ptr(p.scale), _ptr(p.zero),
                        p.cols, p.n_keep, p.group, _ptr(x), m, _ptr(rows),
                        rows.size, _ptr(y))
@@ -265,3 +286,40 @@ def pack_scored(W: np.ndarray, xnorm: np.ndarray, grad, n_keep: int,
     if rc:
         raise OracleError(rc, "pack_scored")
     return Packed(rows, cols, n_keep, group, vals, idx, scale, zero)
+
+
+def pack_rowg(W: np.ndarray, n_keep: int, row_group) -> Packed:
+    """Magnitude pruning and quantisation with a group size per row."""
+    W = _c(W, np.float32)
+    rows, cols = W.shape
+    rg = _c(row_group, np.int32)
+    if rg.shape != (rows,):
+        raise ValueError("one group size per row")
+    vb, ib = row_bytes(cols, n_keep)
+    ng = int(sum(cols // int(g) for g in rg)) if rows else 0
+    vals = np.zeros((rows, vb), dtype=np.uint8)
+    idx = np.zeros((rows, ib), dtype=np.uint8)
+    scale = np.zeros(ng, dtype=np.uint16)
+    zero = np.zeros(ng, dtype=np.uint16)
+    rc = _load().orc_pack_rowg(_ptr(W), rows, cols, n_keep, _ptr(rg), _ptr(vals),
+                               _ptr(idx), _ptr(scale), _ptr(zero))
+    if rc:
+        raise OracleError(rc, "pack_rowg")
+    return Packed(rows, cols, n_keep, None, vals, idx, scale, zero, row_group=rg)
+
+
+def quantize_rowg(W: np.ndarray, pos: np.ndarray, n_keep: int, row_group):
+    W = _c(W, np.float32)
+    pos = _c(pos, np.uint8)
+    rows, cols = W.shape
+    rg = _c(row_group, np.int32)
+    P = cols // 4 * n_keep
+    ng = int(sum(cols // int(g) for g in rg)) if rows else 0
+    q = np.zeros((rows, P), dtype=np.uint8)
+    scale = np.zeros(ng, dtype=np.uint16)
+    zero = np.zeros(ng, dtype=np.uint16)
+    rc = _load().orc_quantize_rowg(_ptr(W), _ptr(pos), rows, cols, n_keep, _ptr(rg),
+                                   _ptr(q), _ptr(scale), _ptr(zero))
+    if rc:
+        raise OracleError(rc, "quantize_rowg")
+    return q, scale, zero

@@ -376,3 +376,85 @@ void orc_matvec(const uint8_t* vals, const uint8_t* idx,
   free(row);
   free(xd);
 }
+
+/* ------------------------------------------------------------------ */
+/* Per-row group sizes (the paper's finer groups for sensitive channels,
+ * section 3.2 "Adaptive group quantization"): row r is quantised with its
+ * own group size row_group[r]; its scale/zero entries follow those of the
+ * rows before it (offset sum_{r' < r} cols / row_group[r']).  Every row is
+ * the single-row case of the functions above.                          */
+/* ------------------------------------------------------------------ */
+
+static int row_groups_ok(const int* row_group, int64_t rows, int64_t cols) {
+  if (!row_group) return 0;
+  for (int64_t r = 0; r < rows; ++r) {
+    int g = row_group[r];
+    if (g <= 0 || cols % g != 0) return 0;
+  }
+  return 1;
+}
+
+int orc_quantize_rowg(const float* W, const uint8_t* pos, int64_t rows,
+                      int64_t cols, int n_keep, const int* row_group,
+                      uint8_t* q, uint16_t* scale, uint16_t* zero) {
+  if (!shape_ok(rows, cols, n_keep) || !row_groups_ok(row_group, rows, cols))
+    return ORC_ERR_ARG;
+  int64_t P = cols / 4 * n_keep, off = 0;
+  for (int64_t r = 0; r < rows; ++r) {
+    int rc = orc_quantize(W + r * cols, pos + r * P, 1, cols, n_keep,
+                          row_group[r], q + r * P, scale + off, zero + off);
+    if (rc != ORC_OK) return rc;
+    off += cols / row_group[r];
+  }
+  return ORC_OK;
+}
+
+int orc_pack_rowg(const float* W, int64_t rows, int64_t cols, int n_keep,
+                  const int* row_group, uint8_t* vals, uint8_t* idx,
+                  uint16_t* scale, uint16_t* zero) {
+  if (!shape_ok(rows, cols, n_keep) || !row_groups_ok(row_group, rows, cols))
+    return ORC_ERR_ARG;
+  int64_t vb = orc_vals_row_bytes(cols, n_keep), ib = orc_idx_row_bytes(cols, n_keep);
+  int64_t off = 0;
+  for (int64_t r = 0; r < rows; ++r) {
+    int rc = orc_pack(W + r * cols, 1, cols, n_keep, row_group[r], vals + r * vb,
+                      idx + r * ib, scale + off, zero + off);
+    if (rc != ORC_OK) return rc;
+    off += cols / row_group[r];
+  }
+  return ORC_OK;
+}
+
+void orc_dequant_rows_rowg(const uint8_t* vals, const uint8_t* idx,
+                           const uint16_t* scale, const uint16_t* zero,
+                           int64_t cols, int n_keep, const int* row_group,
+                           int64_t row0, int64_t nrows, double* out) {
+  int64_t vb = orc_vals_row_bytes(cols, n_keep), ib = orc_idx_row_bytes(cols, n_keep);
+  int64_t off = 0;
+  for (int64_t r = 0; r < row0; ++r) off += cols / row_group[r];
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t r = row0 + i;
+    orc_dequant_rows(vals + r * vb, idx + r * ib, scale + off, zero + off, cols,
+                     n_keep, row_group[r], 0, 1, out + i * cols);
+    off += cols / row_group[r];
+  }
+}
+
+void orc_matvec_rowg(const uint8_t* vals, const uint8_t* idx,
+                     const uint16_t* scale, const uint16_t* zero, int64_t rows,
+                     int64_t cols, int n_keep, const int* row_group,
+                     const uint16_t* x, int m, const int64_t* rows_list,
+                     int64_t n_list, double* y) {
+  int64_t vb = orc_vals_row_bytes(cols, n_keep), ib = orc_idx_row_bytes(cols, n_keep);
+  int64_t* off = (int64_t*)malloc((size_t)(rows + 1) * sizeof(int64_t));
+  if (!off) return;
+  off[0] = 0;
+  for (int64_t r = 0; r < rows; ++r) off[r + 1] = off[r] + cols / row_group[r];
+  const int64_t zero_row = 0;
+  for (int64_t i = 0; i < n_list; ++i) {
+    int64_t r = rows_list[i];
+    orc_matvec(vals + r * vb, idx + r * ib, scale + off[r], zero + off[r], cols,
+               n_keep, row_group[r], x, m, &zero_row, 1, y + i * m);
+  }
+  free(off);
+}

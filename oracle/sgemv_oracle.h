@@ -111,6 +111,26 @@ void orc_matvec(const uint8_t* vals, const uint8_t* idx,
                 int n_keep, int group, const uint16_t* x, int m,
                 const int64_t* rows_list, int64_t n_list, double* y);
 
+/* Per-row group sizes: row r uses group row_group[r] (a divisor of cols);
+ * scale/zero hold each row's cols / row_group[r] entries after those of
+ * the rows before it.  Each row is exactly the single-row case of the
+ * uniform-group functions above. */
+int orc_quantize_rowg(const float* W, const uint8_t* pos, int64_t rows,
+                      int64_t cols, int n_keep, const int* row_group,
+                      uint8_t* q, uint16_t* scale, uint16_t* zero);
+int orc_pack_rowg(const float* W, int64_t rows, int64_t cols, int n_keep,
+                  const int* row_group, uint8_t* vals, uint8_t* idx,
+                  uint16_t* scale, uint16_t* zero);
+void orc_dequant_rows_rowg(const uint8_t* vals, const uint8_t* idx,
+                           const uint16_t* scale, const uint16_t* zero,
+                           int64_t cols, int n_keep, const int* row_group,
+                           int64_t row0, int64_t nrows, double* out);
+void orc_matvec_rowg(const uint8_t* vals, const uint8_t* idx,
+                     const uint16_t* scale, const uint16_t* zero, int64_t rows,
+                     int64_t cols, int n_keep, const int* row_group,
+                     const uint16_t* x, int m, const int64_t* rows_list,
+                     int64_t n_list, double* y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -249,6 +249,83 @@ def test_pack_scored_composes_the_steps(orc):
 
 
 # ---------------------------------------------------------------------------
+# Per-row group sizes (finer groups for sensitive rows inside one layer).
+# ---------------------------------------------------------------------------
+
+def _row_groups(seed, rows, choices=(64, 128, 256)):
+    return np.random.default_rng(seed).choice(choices, rows).astype(np.int32)
+
+
+def test_rowg_uniform_equals_matrix_group(orc):
+    W = synth.weight_outliers(21, 24, 512)
+    for n_keep, g in ((2, 128), (1, 64), (1, 256)):
+        a = orc.pack(W, n_keep, g)
+        b = orc.pack_rowg(W, n_keep, np.full(24, g, np.int32))
+        assert np.array_equal(a.vals, b.vals) and np.array_equal(a.idx, b.idx)
+        assert np.array_equal(a.scale.ravel(), b.scale)
+        assert np.array_equal(a.zero.ravel(), b.zero)
+
+
+@pytest.mark.parametrize("n_keep", [1, 2])
+def test_rowg_rows_are_independent_with_own_group(orc, n_keep):
+    W = synth.weight_outliers(22, 20, 768)
+    rg = _row_groups(3, 20)
+    p = orc.pack_rowg(W, n_keep, rg)
+    off = 0
+    for r in range(20):
+        one = orc.pack(W[r:r + 1], n_keep, int(rg[r]))
+        ng = 768 // int(rg[r])
+        assert np.array_equal(p.vals[r], one.vals[0]) and np.array_equal(p.idx[r], one.idx[0])
+        assert np.array_equal(p.scale[off:off + ng], one.scale[0])
+        assert np.array_equal(p.zero[off:off + ng], one.zero[0])
+        off += ng
+    assert off == p.scale.size
+
+
+def test_rowg_quant_error_bound_per_row_group(orc):
+    """|w - w_hat| <= s of the weight's own (row, group), located with
+    offsets computed here from the row groups."""
+    W = synth.weight_normal(23, 16, 512, 0.02)
+    rg = _row_groups(4, 16)
+    p = orc.pack_rowg(W, 2, rg)
+    dense = orc.dequant(p)
+    pos = orc.prune(W, 2)
+    off = 0
+    for r in range(16):
+        g = int(rg[r])
+        for t in range(128):
+            for a in pos[r, t]:
+                c = 4 * t + int(a)
+                s = orc.f16_bits_to_f64(int(p.scale[off + c // g]))
+                assert abs(float(W[r, c]) - dense[r, c]) <= s
+        off += 512 // g
+
+
+def test_rowg_matvec_closed_forms(orc):
+    W = synth.weight_outliers(24, 12, 256)
+    p = orc.pack_rowg(W, 1, _row_groups(5, 12))
+    dense = orc.dequant(p)
+    ones = np.ones((1, 256), np.float16)
+    y = orc.matvec(p, ones)[0]
+    assert np.array_equal(y, np.array([math.fsum(r) for r in dense]))
+    torch = pytest.importorskip("torch")
+    x = synth.activations(6, 3, 256)
+    ref = (torch.from_numpy(x.astype(np.float64)) @ torch.from_numpy(dense).T).numpy()
+    assert np.allclose(orc.matvec(p, x), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_rowg_quantize_matches_pack(orc):
+    W = synth.weight_normal(25, 10, 384, 0.02)
+    rg = _row_groups(6, 10, (64, 128))
+    pos = orc.prune(W, 2)
+    q, sc, z = orc.quantize_rowg(W, pos, 2, rg)
+    vals, idx = orc.encode(pos, q, 10, 384, 2)
+    p = orc.pack_rowg(W, 2, rg)
+    assert np.array_equal(p.vals, vals) and np.array_equal(p.idx, idx)
+    assert np.array_equal(p.scale, sc) and np.array_equal(p.zero, z)
+
+
+# ---------------------------------------------------------------------------
 # Hand-derived tiny cases: prune + quantise + encode + dequant + matvec.
 # ---------------------------------------------------------------------------
 
