@@ -89,6 +89,23 @@ int sgemv_create(sgemv_t* out, int rows, int cols, int n_keep, int group,
                  int max_m, int device);
 
 /*
+ * As sgemv_create, with a group size per row instead of per matrix: the
+ * paper gives sensitive channels more (finer) groups inside one layer
+ * (section 3.2, "Adaptive group quantization").  row_group (host, rows
+ * entries, read only) holds each row's group size, 64, 128 or 256, each a
+ * divisor of cols.  Row r is quantised exactly as a one-row matrix with
+ * group row_group[r].  The canonical scale and zero arrays of import and
+ * export are then flat: row r's cols / row_group[r] entries follow those of
+ * rows 0..r-1 (sgemv_sizes reports their total).  Every other call works as
+ * for sgemv_create.  In device memory the scale/zero words are kept at the
+ * finest group of the matrix, a coarser group's pair repeated in each of its
+ * sub-groups, so a product reads 4 * cols / min(row_group) bytes of them per
+ * row; sgemv_packed_bytes counts the canonical ones.
+ */
+int sgemv_create_rowgroups(sgemv_t* out, int rows, int cols, int n_keep,
+                           const int* row_group, int max_m, int device);
+
+/*
  * Prune, quantise and pack a dense fp32 weight (rows x cols, row-major,
  * host memory, read only).  The work runs on the handle's device; the call
  * returns when it is done.  NaN/Inf anywhere -> SGEMV_ERR_NONFINITE; a scale

@@ -32,6 +32,7 @@ _SZ = ctypes.c_size_t
 _PSZ = ctypes.POINTER(ctypes.c_size_t)
 SIGNATURES = {
     "sgemv_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _I, _I]),
+    "sgemv_create_rowgroups": (_I, [ctypes.POINTER(_P), _I, _I, _I, _P, _I, _I]),
     "sgemv_pack": (_I, [_P, _P]),
     "sgemv_pack_device": (_I, [_P, _P, _P]),
     "sgemv_pack_scored": (_I, [_P, _P, _P, _P]),
@@ -96,15 +97,27 @@ class SparseGemv:
     """A packed N:4 2bit-CSR INT4 weight on one GPU.
 
     rows x cols is out features x in features; n_keep is N (1 or 2); group
-    is the quantisation group in dense columns (64, 128 or 256).
+    is the quantisation group in dense columns (64, 128 or 256).  With
+    row_group (one size per row) group is None and each row has its own.
     """
 
-    def __init__(self, rows: int, cols: int, n_keep: int, group: int,
-                 max_m: int = 1, device: int = 0):
+    def __init__(self, rows: int, cols: int, n_keep: int, group, max_m: int = 1,
+                 device: int = 0, row_group=None):
         lib = load()
         h = ctypes.c_void_p()
-        _check(lib.sgemv_create(ctypes.byref(h), rows, cols, n_keep, group,
-                                max_m, device), "sgemv_create")
+        self.row_group = None
+        if row_group is not None:
+            rg = np.ascontiguousarray(row_group, dtype=np.int32)
+            if rg.shape != (rows,):
+                raise ValueError(f"row_group shape {rg.shape} != {(rows,)}")
+            _check(lib.sgemv_create_rowgroups(ctypes.byref(h), rows, cols, n_keep,
+                                              rg.ctypes.data, max_m, device),
+                   "sgemv_create_rowgroups")
+            self.row_group = rg
+            group = None
+        else:
+            _check(lib.sgemv_create(ctypes.byref(h), rows, cols, n_keep, group,
+                                    max_m, device), "sgemv_create")
         self._h = h
         self.rows, self.cols, self.n_keep, self.group = rows, cols, n_keep, group
         self.max_m, self.device = max_m, device
@@ -192,11 +205,15 @@ class SparseGemv:
         s = self.sizes()
         vb = s["vals"] // max(self.rows, 1) if self.rows else 0
         ib = s["idx"] // max(self.rows, 1) if self.rows else 0
-        ng = self.cols // self.group
         vals = np.zeros((self.rows, vb), np.uint8)
         idx = np.zeros((self.rows, ib), np.uint8)
-        scale = np.zeros((self.rows, ng), np.uint16)
-        zero = np.zeros((self.rows, ng), np.uint16)
+        if self.row_group is None:
+            ng = self.cols // self.group
+            scale = np.zeros((self.rows, ng), np.uint16)
+            zero = np.zeros((self.rows, ng), np.uint16)
+        else:   # flat: each row's entries after those of the rows before it
+            scale = np.zeros(s["groups"], np.uint16)
+            zero = np.zeros(s["groups"], np.uint16)
         _check(load().sgemv_export(self._h, vals.ctypes.data, idx.ctypes.data,
                                    scale.ctypes.data, zero.ctypes.data),
                "sgemv_export")

@@ -107,6 +107,13 @@ size_t vals_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.cstrid
 size_t idx_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.cstride * 8; }
 size_t sz_dev_bytes(const sgemv::Layout& L) { return (size_t)L.rows * L.gstride * 4; }
 
+sgemv::RowGroups row_groups(sgemv_t h) {
+  sgemv::RowGroups g;
+  g.rowg = h->d_rowg;
+  g.goff = h->d_goff;
+  return g;
+}
+
 void free_ctx(sgemv_t h) {
   if (!h) return;
   cudaFree(h->d_vals);
@@ -115,6 +122,8 @@ void free_ctx(sgemv_t h) {
   cudaFree(h->d_xstage);
   cudaFree(h->d_ystage);
   cudaFree(h->d_err);
+  cudaFree(h->d_rowg);
+  cudaFree(h->d_goff);
   if (h->stream) cudaStreamDestroy(h->stream);
   delete h;
 }
@@ -130,7 +139,7 @@ int pack_on_device(sgemv_t h, const float* w_dev, cudaStream_t s, const float* x
     CUDA_TRY(cudaMemsetAsync(h->d_idx, 0, idx_dev_bytes(L), s), "memset idx");
   if (sz_dev_bytes(L))
     CUDA_TRY(cudaMemsetAsync(h->d_sz, 0, sz_dev_bytes(L), s), "memset scale/zero");
-  CUDA_TRY(sgemv::launch_pack(L, w_dev, xnorm_dev, grad_dev, h->d_vals, h->d_idx, h->d_sz,
+  CUDA_TRY(sgemv::launch_pack(L, row_groups(h), w_dev, xnorm_dev, grad_dev, h->d_vals, h->d_idx, h->d_sz,
                               h->d_err, s),
            "pack kernel");
   CUDA_TRY(cudaStreamSynchronize(s), "pack");
@@ -149,8 +158,11 @@ extern "C" {
 
 const char* sgemv_last_error(void) { return g_err; }
 
-int sgemv_create(sgemv_t* out, int rows, int cols, int n_keep, int group,
-                 int max_m, int device) {
+}  // extern "C"
+
+// Creates a handle; row_group (host, rows entries) optional.
+static int create_impl(sgemv_t* out, int rows, int cols, int n_keep, int group,
+                       const int* row_group, int max_m, int device) {
   if (!out) return fail(SGEMV_ERR_ARG, "out is NULL");
   *out = nullptr;
   if (rows < 0 || rows > SGEMV_MAX_ROWS)
@@ -176,6 +188,7 @@ int sgemv_create(sgemv_t* out, int rows, int cols, int n_keep, int group,
   sgemv_t h = new sgemv_ctx();
   memset(h, 0, sizeof *h);
   h->L = make_layout(rows, cols, n_keep, group);
+  h->canon_groups = (int64_t)rows * h->L.ngroups;
   h->max_m = max_m;
   h->device = device;
   h->ready = false;
@@ -200,12 +213,56 @@ int sgemv_create(sgemv_t* out, int rows, int cols, int n_keep, int group,
     e = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) rc = cuda_fail(e, "cudaStreamCreate");
   }
+  if (!rc && row_group && rows > 0) {
+    // group size per row: device copy and the canonical scale/zero offsets
+    int64_t* off = new int64_t[(size_t)rows + 1];
+    off[0] = 0;
+    for (int r = 0; r < rows; ++r) off[r + 1] = off[r] + cols / row_group[r];
+    h->canon_groups = off[rows];
+    rc = try_alloc((void**)&h->d_rowg, (size_t)rows * sizeof(int), "cudaMalloc row groups");
+    if (!rc) rc = try_alloc((void**)&h->d_goff, ((size_t)rows + 1) * sizeof(int64_t),
+                            "cudaMalloc group offsets");
+    if (!rc) {
+      e = cudaMemcpy(h->d_rowg, row_group, (size_t)rows * sizeof(int), cudaMemcpyHostToDevice);
+      if (e == cudaSuccess)
+        e = cudaMemcpy(h->d_goff, off, ((size_t)rows + 1) * sizeof(int64_t),
+                       cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) rc = cuda_fail(e, "copy row groups");
+    }
+    delete[] off;
+  }
   if (rc) {
     free_ctx(h);
     return rc;
   }
   *out = h;
   return SGEMV_OK;
+}
+
+extern "C" {
+
+int sgemv_create(sgemv_t* out, int rows, int cols, int n_keep, int group,
+                 int max_m, int device) {
+  return create_impl(out, rows, cols, n_keep, group, nullptr, max_m, device);
+}
+
+int sgemv_create_rowgroups(sgemv_t* out, int rows, int cols, int n_keep,
+                           const int* row_group, int max_m, int device) {
+  if (!out) return fail(SGEMV_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  if (rows < 0 || rows > SGEMV_MAX_ROWS)
+    return fail(SGEMV_ERR_ARG, "rows=%d outside [0, %d]", rows, SGEMV_MAX_ROWS);
+  if (rows > 0 && !row_group) return fail(SGEMV_ERR_ARG, "row_group is NULL");
+  int gmin = rows > 0 ? 256 : 64;
+  for (int r = 0; r < rows; ++r) {
+    const int g = row_group[r];
+    if (g != 64 && g != 128 && g != 256)
+      return fail(SGEMV_ERR_ARG, "row_group[%d]=%d: must be 64, 128 or 256", r, g);
+    if (cols % g != 0)
+      return fail(SGEMV_ERR_ARG, "cols=%d is not a multiple of row_group[%d]=%d", cols, r, g);
+    gmin = g < gmin ? g : gmin;
+  }
+  return create_impl(out, rows, cols, n_keep, gmin, row_group, max_m, device);
 }
 
 int sgemv_destroy(sgemv_t h) {
@@ -281,7 +338,7 @@ int sgemv_import(sgemv_t h, const uint8_t* vals, const uint8_t* idx,
   if (int rc = check_handle(h)) return rc;
   const sgemv::Layout& L = h->L;
   const size_t nv = (size_t)L.rows * L.vals_row, ni = (size_t)L.rows * L.idx_row;
-  const size_t ns = (size_t)L.rows * L.ngroups;
+  const size_t ns = (size_t)h->canon_groups;
   if ((nv && !vals) || (ni && !idx) || (ns && (!scale || !zero)))
     return fail(SGEMV_ERR_ARG, "a canonical input pointer is NULL");
   DeviceGuard g(h->device);
@@ -303,7 +360,7 @@ int sgemv_import(sgemv_t h, const uint8_t* vals, const uint8_t* idx,
   if (sz_dev_bytes(L))
     CUDA_TRY(cudaMemsetAsync(h->d_sz, 0, sz_dev_bytes(L), s), "memset scale/zero");
   CUDA_TRY(sgemv::launch_canon_to_device(
-               L, (const uint8_t*)cv.p, (const uint8_t*)ci.p, (const uint16_t*)cs.p,
+               L, row_groups(h), (const uint8_t*)cv.p, (const uint8_t*)ci.p, (const uint16_t*)cs.p,
                (const uint16_t*)cz.p, h->d_vals, h->d_idx, h->d_sz, h->d_err, s),
            "import kernel");
   int rc = collect_dev_err(h);
@@ -317,7 +374,7 @@ int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
   if (!h->ready) return fail(SGEMV_ERR_STATE, "export before pack or import");
   const sgemv::Layout& L = h->L;
   const size_t nv = (size_t)L.rows * L.vals_row, ni = (size_t)L.rows * L.idx_row;
-  const size_t ns = (size_t)L.rows * L.ngroups;
+  const size_t ns = (size_t)h->canon_groups;
   if ((nv && !vals) || (ni && !idx) || (ns && (!scale || !zero)))
     return fail(SGEMV_ERR_ARG, "a canonical output pointer is NULL");
   DeviceGuard g(h->device);
@@ -328,7 +385,7 @@ int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
   CUDA_TRY(cs.alloc(ns * 2), "cudaMalloc");
   CUDA_TRY(cz.alloc(ns * 2), "cudaMalloc");
   cudaStream_t s = h->stream;
-  CUDA_TRY(sgemv::launch_device_to_canon(L, h->d_vals, h->d_idx, h->d_sz,
+  CUDA_TRY(sgemv::launch_device_to_canon(L, row_groups(h), h->d_vals, h->d_idx, h->d_sz,
                                          (uint8_t*)cv.p, (uint8_t*)ci.p,
                                          (uint16_t*)cs.p, (uint16_t*)cz.p, s),
            "export kernel");
@@ -505,7 +562,7 @@ int sgemv_sizes(sgemv_t h, size_t* vals_bytes, size_t* idx_bytes,
   const sgemv::Layout& L = h->L;
   if (vals_bytes) *vals_bytes = (size_t)L.rows * L.vals_row;
   if (idx_bytes) *idx_bytes = (size_t)L.rows * L.idx_row;
-  if (n_groups) *n_groups = (size_t)L.rows * L.ngroups;
+  if (n_groups) *n_groups = (size_t)h->canon_groups;
   if (device_bytes) *device_bytes = vals_dev_bytes(L) + idx_dev_bytes(L) + sz_dev_bytes(L);
   return SGEMV_OK;
 }
@@ -514,7 +571,7 @@ size_t sgemv_packed_bytes(sgemv_t h) {
   if (!h) return 0;
   const sgemv::Layout& L = h->L;
   const size_t kept = (size_t)L.rows * L.kept;
-  return kept / 2 + kept / 4 + (size_t)L.rows * L.ngroups * 4;
+  return kept / 2 + kept / 4 + (size_t)h->canon_groups * 4;
 }
 
 }  // extern "C"

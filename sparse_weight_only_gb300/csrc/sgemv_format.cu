@@ -48,7 +48,8 @@ __device__ __forceinline__ void prune_quad(const float w[4], const float a[4], i
 // 3.2): |w| * xnorm[col] + |w| * |grad| (grad NULL: zero gradient), two
 // products and a sum each rounded once in binary32, as written.
 template <int N>
-__global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict__ w,
+__global__ void __launch_bounds__(256) k_pack(Layout L, RowGroups RG, int seg_max,
+                                             const float* __restrict__ w,
                                              const float* __restrict__ xnorm,
                                              const float* __restrict__ grad,
                                              uint8_t* __restrict__ vals,
@@ -61,7 +62,8 @@ __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict_
   const bool active = u < total;
   const int64_t r = active ? u / upr : 0;
   const int64_t k = active ? u % upr : 0;
-  const int seg = L.group / 16;                       // threads per group
+  const int gr = RG.rowg && active ? RG.rowg[r] : L.group;   // this row's group size
+  const int seg = gr / 16;                            // threads per group
 
   float wv[16];
   if (active) {
@@ -121,9 +123,16 @@ __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict_
       hi = fmaxf(hi, val[t][n]);
     }
   }
-  for (int off = 1; off < seg; off <<= 1) {
-    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+  // groups are seg-aligned runs of lanes (a row's units start at a multiple
+  // of cols/16, a multiple of seg); every lane joins every shuffle and keeps
+  // only partners of its own group
+  for (int off = 1; off < seg_max; off <<= 1) {
+    const float olo = __shfl_xor_sync(0xffffffffu, lo, off);
+    const float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+    if (off < seg) {
+      lo = fminf(lo, olo);
+      hi = fmaxf(hi, ohi);
+    }
   }
   if (!active || bad) return;
 
@@ -183,10 +192,11 @@ __global__ void __launch_bounds__(256) k_pack(Layout L, const float* __restrict_
     *reinterpret_cast<uint16_t*>(vals + r * vrow + 2 * k) = (uint16_t)vw;
     idx[r * irow + k] = (uint8_t)iw;
   }
-  if ((threadIdx.x & (seg - 1)) == 0) {
-    const int64_t G = (16 * k) / L.group;
+  // the thread at the start of each device group (L.group columns; a row's
+  // coarser group covers several) writes the group's scale and zero there
+  if ((16 * k) % L.group == 0) {
     const unsigned short z16 = __half_as_ushort(__float2half_rn(zfl));
-    sz[r * L.gstride + G] = (uint32_t)s16 | ((uint32_t)z16 << 16);
+    sz[r * L.gstride + (16 * k) / L.group] = (uint32_t)s16 | ((uint32_t)z16 << 16);
   }
 }
 
@@ -232,24 +242,31 @@ __global__ void k_canon_to_device(Layout L, const uint8_t* __restrict__ cvals,
   }
 }
 
-__global__ void k_sz_to_device(Layout L, const uint16_t* __restrict__ scale,
+// One thread per (row, device group of L.group columns).  The canonical
+// entry of device group Gd of row r is its row group Gd * L.group / g_r.
+__global__ void k_sz_to_device(Layout L, RowGroups RG, const uint16_t* __restrict__ scale,
                                const uint16_t* __restrict__ zero,
                                uint32_t* __restrict__ sz) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)L.rows * L.ngroups) return;
-  const int64_t r = i / L.ngroups, G = i % L.ngroups;
-  sz[r * L.gstride + G] = (uint32_t)scale[i] | ((uint32_t)zero[i] << 16);
+  const int64_t r = i / L.ngroups, Gd = i % L.ngroups;
+  const int gr = RG.rowg ? RG.rowg[r] : L.group;
+  const int64_t ci = (RG.goff ? RG.goff[r] : r * L.ngroups) + Gd * L.group / gr;
+  sz[r * L.gstride + Gd] = (uint32_t)scale[ci] | ((uint32_t)zero[ci] << 16);
 }
 
-__global__ void k_sz_to_canon(Layout L, const uint32_t* __restrict__ sz,
+__global__ void k_sz_to_canon(Layout L, RowGroups RG, const uint32_t* __restrict__ sz,
                               uint16_t* __restrict__ scale,
                               uint16_t* __restrict__ zero) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)L.rows * L.ngroups) return;
-  const int64_t r = i / L.ngroups, G = i % L.ngroups;
-  const uint32_t w = sz[r * L.gstride + G];
-  scale[i] = (uint16_t)(w & 0xFFFFu);
-  zero[i] = (uint16_t)(w >> 16);
+  const int64_t r = i / L.ngroups, Gd = i % L.ngroups;
+  const int gr = RG.rowg ? RG.rowg[r] : L.group;
+  if ((Gd * L.group) % gr != 0) return;   // not the first sub-slot of its row group
+  const int64_t ci = (RG.goff ? RG.goff[r] : r * L.ngroups) + Gd * L.group / gr;
+  const uint32_t w = sz[r * L.gstride + Gd];
+  scale[ci] = (uint16_t)(w & 0xFFFFu);
+  zero[ci] = (uint16_t)(w >> 16);
 }
 
 // Device -> canonical: one thread per (row, chunk).
@@ -283,21 +300,23 @@ inline unsigned blocks_for(int64_t n, int threads) {
 
 }  // namespace
 
-cudaError_t launch_pack(const Layout& L, const float* w, const float* xnorm, const float* grad,
-                        uint4* vals, uint2* idx, uint32_t* sz, int* err, cudaStream_t s) {
+cudaError_t launch_pack(const Layout& L, const RowGroups& G, const float* w, const float* xnorm,
+                        const float* grad, uint4* vals, uint2* idx, uint32_t* sz, int* err,
+                        cudaStream_t s) {
   const int64_t total = (int64_t)L.rows * (L.cols / 16);
   if (total == 0) return cudaSuccess;
   const unsigned nb = blocks_for(total, 256);
+  const int seg_max = G.rowg ? 16 : L.group / 16;
   if (L.n_keep == 2)
-    k_pack<2><<<nb, 256, 0, s>>>(L, w, xnorm, grad, reinterpret_cast<uint8_t*>(vals),
+    k_pack<2><<<nb, 256, 0, s>>>(L, G, seg_max, w, xnorm, grad, reinterpret_cast<uint8_t*>(vals),
                                  reinterpret_cast<uint8_t*>(idx), sz, err);
   else
-    k_pack<1><<<nb, 256, 0, s>>>(L, w, xnorm, grad, reinterpret_cast<uint8_t*>(vals),
+    k_pack<1><<<nb, 256, 0, s>>>(L, G, seg_max, w, xnorm, grad, reinterpret_cast<uint8_t*>(vals),
                                  reinterpret_cast<uint8_t*>(idx), sz, err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_canon_to_device(const Layout& L, const uint8_t* cvals,
+cudaError_t launch_canon_to_device(const Layout& L, const RowGroups& G, const uint8_t* cvals,
                                    const uint8_t* cidx, const uint16_t* scale,
                                    const uint16_t* zero, uint4* vals, uint2* idx,
                                    uint32_t* sz, int* err, cudaStream_t s) {
@@ -313,11 +332,11 @@ cudaError_t launch_canon_to_device(const Layout& L, const uint8_t* cvals,
           reinterpret_cast<uint8_t*>(idx), err);
   }
   const int64_t ns = (int64_t)L.rows * L.ngroups;
-  if (ns > 0) k_sz_to_device<<<blocks_for(ns, 256), 256, 0, s>>>(L, scale, zero, sz);
+  if (ns > 0) k_sz_to_device<<<blocks_for(ns, 256), 256, 0, s>>>(L, G, scale, zero, sz);
   return cudaGetLastError();
 }
 
-cudaError_t launch_device_to_canon(const Layout& L, const uint4* vals,
+cudaError_t launch_device_to_canon(const Layout& L, const RowGroups& G, const uint4* vals,
                                    const uint2* idx, const uint32_t* sz,
                                    uint8_t* cvals, uint8_t* cidx, uint16_t* scale,
                                    uint16_t* zero, cudaStream_t s) {
@@ -333,7 +352,7 @@ cudaError_t launch_device_to_canon(const Layout& L, const uint4* vals,
           reinterpret_cast<const uint8_t*>(idx), cvals, cidx);
   }
   const int64_t ns = (int64_t)L.rows * L.ngroups;
-  if (ns > 0) k_sz_to_canon<<<blocks_for(ns, 256), 256, 0, s>>>(L, sz, scale, zero);
+  if (ns > 0) k_sz_to_canon<<<blocks_for(ns, 256), 256, 0, s>>>(L, G, sz, scale, zero);
   return cudaGetLastError();
 }
 

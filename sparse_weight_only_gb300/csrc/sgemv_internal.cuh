@@ -56,6 +56,13 @@ struct sgemv_ctx {
   __half* d_ystage;    // max_m x rows
   int* d_err;          // device error word
   cudaStream_t stream; // private stream for pack / import / export
+  // group size per row (NULL: every row uses L.group).  With per-row sizes
+  // L.group is the finest of them and the device keeps scale/zero at that
+  // granularity, a coarser group's words repeated in each of its sub-slots,
+  // so the product kernels index groups uniformly.
+  int* d_rowg;         // rows group sizes
+  int64_t* d_goff;     // rows + 1 canonical scale/zero offsets
+  int64_t canon_groups;  // canonical scale/zero entries of the whole matrix
 };
 
 namespace sgemv {
@@ -67,15 +74,23 @@ constexpr int kDevErrBadIndex = 3;
 constexpr int kDevErrTimeout = 4;
 
 // ---- format kernels (sgemv_format.cu) ----
+// Per-row group sizes of a matrix (rowg NULL: L.group for every row) and
+// the canonical scale/zero offset of each row (goff NULL: r * L.ngroups).
+struct RowGroups {
+  const int* rowg;
+  const int64_t* goff;
+};
+
 // xnorm (cols values) selects Eq. 3 importance pruning, with grad (rows x
 // cols) or a zero gradient when grad is NULL; xnorm NULL: magnitude pruning.
-cudaError_t launch_pack(const Layout& L, const float* w, const float* xnorm, const float* grad,
-                        uint4* vals, uint2* idx, uint32_t* sz, int* err, cudaStream_t s);
-cudaError_t launch_canon_to_device(const Layout& L, const uint8_t* cvals,
+cudaError_t launch_pack(const Layout& L, const RowGroups& G, const float* w, const float* xnorm,
+                        const float* grad, uint4* vals, uint2* idx, uint32_t* sz, int* err,
+                        cudaStream_t s);
+cudaError_t launch_canon_to_device(const Layout& L, const RowGroups& G, const uint8_t* cvals,
                                    const uint8_t* cidx, const uint16_t* scale,
                                    const uint16_t* zero, uint4* vals, uint2* idx,
                                    uint32_t* sz, int* err, cudaStream_t s);
-cudaError_t launch_device_to_canon(const Layout& L, const uint4* vals,
+cudaError_t launch_device_to_canon(const Layout& L, const RowGroups& G, const uint4* vals,
                                    const uint2* idx, const uint32_t* sz,
                                    uint8_t* cvals, uint8_t* cidx, uint16_t* scale,
                                    uint16_t* zero, cudaStream_t s);
