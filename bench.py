@@ -479,8 +479,10 @@ def run_ours(args, rank, world, local):
     # small-M verification batches (beam / prefix-tree nodes): the config-4
     # layer set, all 2:4 g = 128, x with M rows; bytes and kept-weight flops
     batch = None
+    rowg = None
     if not args.no_batch:
         batch = run_batch_sweep(args, swo, dev, stream, l2)
+        rowg = run_rowgroup_case(args, swo, dev, stream, l2)
 
     # end to end through the public host-buffer call: H2D x, kernels, D2H y
     xh = [torch.from_numpy(gv.x(m)).pin_memory() for gv in gvs]
@@ -556,6 +558,7 @@ def run_ours(args, rank, world, local):
                                   if isinstance(dense_us, float) else None),
         "pack_seconds": round(t_pack, 3),
         "batch_m": batch,
+        "row_groups": rowg,
         "copies_identical_y": same,
         "launch_mode": ("grouped calls: run_group(q,k,v), run(o), run_group(gate,up), "
                         "run(down)" if grouped else "per-matrix calls"),
@@ -624,6 +627,56 @@ def run_batch_sweep(args, swo, dev, stream, l2):
         del g
     for st in sets:
         for h in st:
+            h.close()
+    return out
+
+
+def run_rowgroup_case(args, swo, dev, stream, l2):
+    """M = 1 on an 11008 x 4096 2:4 layer with a seeded group size per row
+    (64 / 128 / 256), next to the same layer with one group size."""
+    import torch
+    rows, cols = 11008, 4096
+    W = synth.weight_normal(args.seed + 101, rows, cols, 0.02)
+    rg = synth.row_groups(args.seed, rows)
+    x = torch.from_numpy(synth.activations(args.seed + 102, 1, cols)).to(dev)
+    y = torch.empty((1, rows), dtype=torch.float16, device=dev)
+    sptr = stream.cuda_stream
+    out = {"shape": [rows, cols], "n_keep": 2,
+           "rows_per_group": {str(g): int((rg == g).sum()) for g in (64, 128, 256)}}
+    for name, kw in (("per_row", {"row_group": rg}), ("g64", {}), ("g128", {})):
+        group = None if kw else int(name[1:])
+        h0 = swo.SparseGemv(rows, cols, 2, group, device=dev.index, **kw)
+        h0.pack(W)
+        canon = h0.export_canonical()
+        pb = h0.packed_bytes()
+        copies = max(2, math.ceil(4 * l2 / pb) + 1)
+        hs = [h0]
+        for _ in range(copies - 1):
+            h = swo.SparseGemv(rows, cols, 2, group, device=dev.index, **kw)
+            h.import_canonical(*canon)
+            hs.append(h)
+        g = torch.cuda.CUDAGraph()
+        reps = 4 * copies
+        with torch.cuda.stream(stream):
+            hs[0].run(x, y, sptr)
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(reps):
+                    hs[k % copies].run(x, y, sptr)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(5):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (5 * reps)
+        b = pb + 2 * cols + 2 * rows
+        out[name] = {"us": round(us, 3), "bytes": b, "gbs": round(b / us / 1e3, 1)}
+        del g
+        for h in hs:
             h.close()
     return out
 

@@ -179,3 +179,10 @@ def config5(seed: int = 0):
 
 CONFIGS = {"1": config1, "2": config2, "3": config3, "4": config4,
            "5": config5}
+
+
+def row_groups(seed: int, rows: int, choices=(64, 128, 256)) -> np.ndarray:
+    """A group size per row drawn uniformly from `choices` (the stand-in for
+    per-channel sensitivity: finer groups for some rows of a layer)."""
+    rng = np.random.default_rng([seed, 0x52475250])
+    return rng.choice(np.asarray(choices), rows).astype(np.int32)
