@@ -244,13 +244,14 @@ __device__ __forceinline__ float sz_zero(uint32_t w) {
   return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
 }
 
-// Contribution of one chunk (32 kept weights) of one row.  G2: the chunk
-// spans two (scale, zero) groups (1:4 with 64-column groups), units 0..7
-// in the first and 8..15 in the second.
+// acc plus the contribution of one chunk (32 kept weights) of one row, the
+// group scale applied by explicit FMAs so that a row rounds the same way in
+// every launch mode.  G2: the chunk spans two (scale, zero) groups (1:4 with
+// 64-column groups), units 0..7 in the first and 8..15 in the second.
 template <int N, bool G2>
 __device__ __forceinline__ float chunk_dot(const uint4& v, const uint2& ix,
                                            uint32_t sa, uint32_t sb, uint32_t base,
-                                           uint32_t magic) {
+                                           uint32_t magic, float acc) {
   constexpr int E = M1Cfg<N>::E, O = M1Cfg<N>::OFF0;
   float2 a0, a1, a2, a3;
   if (!G2) {
@@ -259,12 +260,12 @@ __device__ __forceinline__ float chunk_dot(const uint4& v, const uint2& ix,
     word_fma<E, O, 4, false>(v.y, ix.x >> 16, base, magic, k, a0, a1, a2, a3);
     word_fma<E, O, 8, false>(v.z, ix.y, base, magic, k, a0, a1, a2, a3);
     word_fma<E, O, 12, false>(v.w, ix.y >> 16, base, magic, k, a0, a1, a2, a3);
-    return sz_scale(sa) * fold(a0, a1, a2, a3);
+    return fmaf(sz_scale(sa), fold(a0, a1, a2, a3), acc);
   } else {
     const ZConst ka = zconst(sz_zero(sa));
     word_fma<E, O, 0, true>(v.x, ix.x, base, magic, ka, a0, a1, a2, a3);
     word_fma<E, O, 4, false>(v.y, ix.x >> 16, base, magic, ka, a0, a1, a2, a3);
-    const float ya = sz_scale(sa) * fold(a0, a1, a2, a3);
+    const float ya = fmaf(sz_scale(sa), fold(a0, a1, a2, a3), acc);
     const ZConst kb = zconst(sz_zero(sb));
     word_fma<E, O, 8, true>(v.z, ix.y, base, magic, kb, a0, a1, a2, a3);
     word_fma<E, O, 12, false>(v.w, ix.y >> 16, base, magic, kb, a0, a1, a2, a3);
@@ -524,11 +525,11 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
         st = st + 1 == kS ? 0 : st + 1;
         if constexpr (N == 1 && MODE == kMany) {
           if (g64)
-            acc += chunk_dot<N, true>(v, ix, sa, sb, tb, magic);
+            acc = chunk_dot<N, true>(v, ix, sa, sb, tb, magic, acc);
           else
-            acc += chunk_dot<N, false>(v, ix, sa, sb, tb, magic);
+            acc = chunk_dot<N, false>(v, ix, sa, sb, tb, magic, acc);
         } else {
-          acc += chunk_dot<N, N == 1 && MODE == kOneG64>(v, ix, sa, sb, tb, magic);
+          acc = chunk_dot<N, N == 1 && MODE == kOneG64>(v, ix, sa, sb, tb, magic, acc);
         }
       }
 #pragma unroll
