@@ -479,9 +479,12 @@ def run_ours(args, rank, world, local):
     # small-M verification batches (beam / prefix-tree nodes): the config-4
     # layer set, all 2:4 g = 128, x with M rows; bytes and kept-weight flops
     batch = None
+    batch_mixed = None
     rowg = None
     if not args.no_batch:
         batch = run_batch_sweep(args, swo, dev, stream, l2)
+        # the same verification batches on the mixed (N, g) layer set
+        batch_mixed = run_batch_sweep(args, swo, dev, stream, l2, gvs, (4, 16, 64))
         rowg = run_rowgroup_case(args, swo, dev, stream, l2)
 
     # end to end through the public host-buffer call: H2D x, kernels, D2H y
@@ -558,6 +561,7 @@ def run_ours(args, rank, world, local):
                                   if isinstance(dense_us, float) else None),
         "pack_seconds": round(t_pack, 3),
         "batch_m": batch,
+        "batch_m_layerset": batch_mixed,
         "row_groups": rowg,
         "copies_identical_y": same,
         "launch_mode": ("grouped calls: run_group(q,k,v), run(o), run_group(gate,up), "
@@ -569,11 +573,13 @@ def run_ours(args, rank, world, local):
     return 0
 
 
-def run_batch_sweep(args, swo, dev, stream, l2):
-    """us and GB/s per M for the config-4 set (seven 2:4 g128 matrices)."""
+def run_batch_sweep(args, swo, dev, stream, l2, gvs=None, ms=None):
+    """us and GB/s per M for the config-4 set (seven 2:4 g128 matrices), or
+    for the given matrices and M values."""
     import torch
-    gvs = synth.config4(args.seed)
-    mmax = max(synth.CONFIG4_M)
+    gvs = synth.config4(args.seed) if gvs is None else gvs
+    ms = synth.CONFIG4_M if ms is None else ms
+    mmax = max(ms)
     hs0 = []
     for gv in gvs:
         W = gv.weight()
@@ -596,7 +602,7 @@ def run_batch_sweep(args, swo, dev, stream, l2):
         sets.append(cp)
     sptr = stream.cuda_stream
     out = {}
-    for m in synth.CONFIG4_M:
+    for m in ms:
         xs = [torch.from_numpy(gv.x(m)).to(dev) for gv in gvs]
         ys = [torch.empty((m, gv.rows), dtype=torch.float16, device=dev) for gv in gvs]
         g = torch.cuda.CUDAGraph()
