@@ -399,10 +399,6 @@ int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
   return SGEMV_OK;
 }
 
-#ifndef SGEMV_M1_ROWLOOP_MAX
-#define SGEMV_M1_ROWLOOP_MAX 64
-#endif
-
 static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s) {
   const sgemv::Layout& L = h->L;
   sgemv::RunArgs a;
@@ -414,25 +410,10 @@ static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s)
   a.m = m;
   a.err = h->d_err;
   if (m == 0 || L.rows == 0) return SGEMV_OK;
-  // m = 1: the CUDA-core table kernel; 2:4 with m >= 2: the sparse tensor
-  // core kernel; 1:4 with a few rows: the table kernel once per activation
-  // row (the weight is re-read per row, from L2 when it fits there);
-  // anything else: the general kernel
-  cudaError_t e = cudaErrorNotSupported;
-  if (m == 1) {
-    e = sgemv::launch_m1(L, a, s);
-  } else if (L.n_keep == 2) {
-    e = sgemv::launch_mma(L, a, s);
-  } else if (m <= SGEMV_M1_ROWLOOP_MAX) {
-    for (int mm = 0; mm < m; ++mm) {
-      sgemv::RunArgs r = a;
-      r.x = a.x + (size_t)mm * L.cols;
-      r.y = a.y + (size_t)mm * L.rows;
-      r.m = 1;
-      e = sgemv::launch_m1(L, r, s);
-      if (e != cudaSuccess) break;
-    }
-  }
+  // m = 1: the CUDA-core table kernel; m >= 2: the sparse tensor-core kernel
+  // (1:4 as 2:4 with a zero partner per quad); anything they do not cover:
+  // the general kernel
+  cudaError_t e = m == 1 ? sgemv::launch_m1(L, a, s) : sgemv::launch_mma(L, a, s);
   if (e == cudaErrorNotSupported) {
     (void)cudaGetLastError();
     e = sgemv::launch_generic(L, a, s);

@@ -1,6 +1,6 @@
 // sgemv_mma.cu -- SparseGemv for a small batch of activation rows on the
-// tensor cores: 2:4 weights, 2 <= m <= 64 (beam candidates / prefix-tree
-// verification nodes).
+// tensor cores: 2 <= m <= 64 (beam candidates / prefix-tree verification
+// nodes), 2:4 weights and 1:4 weights (each kept weight paired with a zero).
 //
 // Product (Dong et al., arXiv 2605.11582, section 1 contribution 2 and
 // section 3.3, applied to the verification batch of section 3.1):
@@ -63,6 +63,7 @@ struct MmaParams {
   int nsplit;         // cluster size
   int sub_chunks;     // chunks of weights and x staged at a time
   int sub_groups;     // scale/zero words per row staged per sub-slice (bound)
+  int ngroups;        // scale/zero groups per row
 };
 
 // half2 (q_a - z, q_b - z) of the quad whose byte is byte `t` of `w`.
@@ -122,6 +123,35 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
+}
+
+// 1:4 operand of quads t and t + 4 of k-step kt for one row, as two half2
+// MMA registers.  Each kept weight is paired with a zero at the other
+// position of its half of the quad -- positions (0, 1) for a < 2, (2, 3)
+// otherwise -- so the 2:4 sparse MMA computes exactly its product; the
+// value sits in the low half for even a and the high half for odd a.  w is
+// vals word kt (quads 8kt .. 8kt + 7, one code per nibble); pw the
+// positions shifted so that quad t's are bits 0..1 and quad t + 4's bits
+// 8..9; z1024 = (1024 + z, 1024 + z).
+__device__ __forceinline__ void quads14(uint32_t w, int t, uint32_t pw, uint32_t z1024,
+                                        uint32_t& r_t, uint32_t& r_t4) {
+  uint32_t h;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(h) : "r"(w >> (4 * t)));
+  uint32_t v;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(h), "r"(z1024));   // (v_t, v_t4)
+  r_t = __byte_perm(v, 0u, 0x4410u - (pw & 1u) * 0x33CCu);
+  r_t4 = __byte_perm(v, 0u, 0x4432u - ((pw >> 8) & 1u) * 0x11EEu);
+}
+
+// 1:4 metadata of MMA quads 4t'..4t'+3 (t' = t % 2): e holds the position
+// byte of those quads for row g (bits 0..7) and row g + 8 (bits 16..23).
+// A position a selects the pair (0, 1) when a < 2 and (2, 3) otherwise:
+// nibble 4 or 14 -- 4 | 10 h with h the high bit of a.
+__device__ __forceinline__ uint32_t meta14(uint32_t e) {
+  e &= 0x00AA00AAu;                                          // h at bits 1, 3, 5, 7
+  uint32_t x = (e & 0x000A000Au) | ((e & 0x00A000A0u) << 4); // -> 1, 3, 9, 11
+  x = (x & 0x02020202u) | ((x & 0x08080808u) << 2);          // -> 1, 5, 9, 13
+  return x | (x << 2) | 0x44444444u;
 }
 
 // (scale as float, (1024 + z, 64 + z) as half2) of one (row, group).
@@ -187,15 +217,17 @@ __device__ __forceinline__ void stage_weights(const MmaParams& p, const WGeom& W
                 p.sz + (size_t)(row0 + w.r) * p.gstride + g0 + w.c);
 }
 
-template <int NT>
+template <int NT, int N>
 __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
+  constexpr int CPC = N == 2 ? 64 : 128;   // dense columns per chunk
+  constexpr int KT = CPC / 32;             // MMA k-steps per chunk
   extern __shared__ __align__(128) unsigned char smem[];
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int mp = NT * 8;                       // padded activation rows
-  const int xs_stride = p.sub_chunks * 64 + 8; // halves per staged x row
+  const int xs_stride = p.sub_chunks * CPC + 8; // halves per staged x row
   const WGeom W(p.sub_chunks, p.sub_groups);
   // shared memory: x of the sub-slice | two weight buffers; after the main
   // loop the partial tile for the cluster reduction reuses the front
@@ -235,8 +267,8 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   // weights of the first sub-slice: in flight while x is staged
   if (nsub > 0) {
     const int ce = min(c_end, c_begin + p.sub_chunks);
-    stage_weights(p, W, wbuf0, row0, c_begin, ce, (c_begin * 64) >> p.gshift,
-                  (ce * 64 - 1) >> p.gshift);
+    stage_weights(p, W, wbuf0, row0, c_begin, ce, (c_begin * CPC) >> p.gshift,
+                  min(p.ngroups - 1, (ce * CPC - 1) >> p.gshift));
   }
   cp_commit();
   // x may be written by the previous kernel: wait for it only now
@@ -246,21 +278,22 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   for (int sidx = 0; sidx < nsub; ++sidx) {
     const int cs = c_begin + sidx * p.sub_chunks;
     const int ce = min(c_end, cs + p.sub_chunks);
-    const int g0 = (cs * 64) >> p.gshift;
+    const int g0 = (cs * CPC) >> p.gshift;
     const uint32_t wb = wbuf0 + (uint32_t)((sidx & 1) * W.bytes);
     __syncthreads();  // previous sub-slice fully consumed: x and the other buffer are free
     if (sidx + 1 < nsub) {
       const int ns = ce, ne = min(c_end, ns + p.sub_chunks);
       stage_weights(p, W, wbuf0 + (uint32_t)(((sidx + 1) & 1) * W.bytes), row0, ns, ne,
-                    (ns * 64) >> p.gshift, (ne * 64 - 1) >> p.gshift);
+                    (ns * CPC) >> p.gshift, min(p.ngroups - 1, (ne * CPC - 1) >> p.gshift));
     }
     cp_commit();
     {
-      // stage x[:, 64 cs .. 64 ce) (zero for padded rows)
-      for (Walk2D w((ce - cs) * 8); w.r < mp; w.step()) {
+      // stage x[:, CPC cs .. CPC ce) (zero for padded rows and past cols)
+      for (Walk2D w((ce - cs) * (CPC / 8)); w.r < mp; w.step()) {
         uint4 q = make_uint4(0, 0, 0, 0);
-        if (w.r < p.m)
-          q = *reinterpret_cast<const uint4*>(p.x + (size_t)w.r * p.cols + cs * 64 + w.c * 8);
+        const int col = cs * CPC + w.c * 8;
+        if (w.r < p.m && col < p.cols)
+          q = *reinterpret_cast<const uint4*>(p.x + (size_t)w.r * p.cols + col);
         *reinterpret_cast<uint4*>(xs + w.r * xs_stride + w.c * 8) = q;
       }
     }
@@ -279,8 +312,9 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
         i_g8 = lds64(wb + W.idx_off + lr_g8 * W.ist + cc * 8);
       }
 #pragma unroll
-      for (int kt = 0; kt < 2; ++kt) {
-        const int G = (c * 64 + kt * 32) >> p.gshift;
+      for (int kt = 0; kt < KT; ++kt) {
+        if (N == 1 && c * CPC + kt * 32 >= p.cols) break;   // ragged 1:4 tail
+        const int G = (c * CPC + kt * 32) >> p.gshift;
         if (G != cur_group) {
           if (cur_group >= 0) {
 #pragma unroll
@@ -298,16 +332,33 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
           group_consts(w_g, s_g, zc_g);
           group_consts(w_g8, s_g8, zc_g8);
         }
-        const uint32_t wlo_g = kt ? v_g.z : v_g.x, whi_g = kt ? v_g.w : v_g.y;
-        const uint32_t wlo_g8 = kt ? v_g8.z : v_g8.x, whi_g8 = kt ? v_g8.w : v_g8.y;
-        const uint32_t a0 = quad_h2(wlo_g, sel, zc_g);    // row g,   quad t
-        const uint32_t a1 = quad_h2(wlo_g8, sel, zc_g8);  // row g+8, quad t
-        const uint32_t a2 = quad_h2(whi_g, sel, zc_g);    // row g,   quad t+4
-        const uint32_t a3 = quad_h2(whi_g8, sel, zc_g8);  // row g+8, quad t+4
-        // metadata (threads t = 0, 1): the stored position nibbles of quads
-        // 4t..4t+3 of this k-tile, row g in the low half, row g+8 in the high
-        const uint32_t meta = __byte_perm(kt ? i_g.y : i_g.x, kt ? i_g8.y : i_g8.x, msel);
-        const uint32_t kofs = (uint32_t)((cc * 64 + kt * 32) * 2);
+        uint32_t a0, a1, a2, a3, meta;
+        if constexpr (N == 2) {
+          const uint32_t wlo_g = kt ? v_g.z : v_g.x, whi_g = kt ? v_g.w : v_g.y;
+          const uint32_t wlo_g8 = kt ? v_g8.z : v_g8.x, whi_g8 = kt ? v_g8.w : v_g8.y;
+          a0 = quad_h2(wlo_g, sel, zc_g);    // row g,   quad t
+          a1 = quad_h2(wlo_g8, sel, zc_g8);  // row g+8, quad t
+          a2 = quad_h2(whi_g, sel, zc_g);    // row g,   quad t+4
+          a3 = quad_h2(whi_g8, sel, zc_g8);  // row g+8, quad t+4
+          // metadata (threads t = 0, 1): the stored position nibbles of quads
+          // 4t..4t+3 of this k-tile, row g in the low half, row g+8 in the high
+          meta = __byte_perm(kt ? i_g.y : i_g.x, kt ? i_g8.y : i_g8.x, msel);
+        } else {
+          // quads 8kt + t and 8kt + t + 4: vals word kt, positions in idx word
+          // kt / 2 from bit 16 (kt % 2) + 2t
+          const uint32_t w_g = kt == 0 ? v_g.x : kt == 1 ? v_g.y : kt == 2 ? v_g.z : v_g.w;
+          const uint32_t w_g8 = kt == 0 ? v_g8.x : kt == 1 ? v_g8.y : kt == 2 ? v_g8.z : v_g8.w;
+          const uint32_t iw_g = kt < 2 ? i_g.x : i_g.y, iw_g8 = kt < 2 ? i_g8.x : i_g8.y;
+          const int sh = 16 * (kt & 1) + 2 * t;
+          // (1024 + z) in both halves: the high half of zc is 64 + z
+          const uint32_t z1024_g = __byte_perm(zc_g, 0u, 0x1010u);
+          const uint32_t z1024_g8 = __byte_perm(zc_g8, 0u, 0x1010u);
+          quads14(w_g, t, iw_g >> sh, z1024_g, a0, a2);
+          quads14(w_g8, t, iw_g8 >> sh, z1024_g8, a1, a3);
+          const uint32_t bi = 2 * (kt & 1) + (t & 1);   // position byte of quads 4t'..4t'+3
+          meta = meta14(__byte_perm(iw_g, iw_g8, bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12)));
+        }
+        const uint32_t kofs = (uint32_t)((cc * CPC + kt * 32) * 2);
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           uint32_t b0, b1, b2, b3;
@@ -363,18 +414,19 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   cluster.sync();  // no CTA leaves while its partial tile is being read
 }
 
-// Shared memory of a launch with sub-slices of `sc` chunks.
-size_t mma_smem(int nt, int sc, int group) {
+// Shared memory of a launch with sub-slices of `sc` chunks of `cpc` columns.
+size_t mma_smem(int nt, int sc, int group, int cpc) {
   const int mp = nt * 8;
-  const WGeom W(sc, (sc * 64 + group - 1) / group + 1);
-  const size_t xs = ((size_t)mp * (sc * 64 + 8) * 2 + 127) & ~(size_t)127;
+  const WGeom W(sc, (sc * cpc + group - 1) / group + 1);
+  const size_t xs = ((size_t)mp * (sc * cpc + 8) * 2 + 127) & ~(size_t)127;
   const size_t main = xs + 2 * (size_t)W.bytes;
   const size_t red = (size_t)kRowsCta * mp * 4;
   return main > red ? main : red;
 }
 
-template <int NT>
+template <int NT, int N>
 cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms) {
+  constexpr int CPC = N == 2 ? 64 : 128;
   const int chunks = (int)L.chunks;
   const int ntiles = (L.rows + kRowsCta - 1) / kRowsCta;
 #ifndef SGEMV_MMA_CTAS_PER_SM
@@ -387,8 +439,8 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
   nsplit = (chunks + split_chunks - 1) / split_chunks;
   // sub-slices: as many chunks as fit two CTAs per SM
   int sub = min(split_chunks, 64);
-  while (sub > 1 && mma_smem(NT, sub, L.group) > kSmemPerCta) sub = (sub + 1) / 2;
-  const size_t smem = mma_smem(NT, sub, L.group);
+  while (sub > 1 && mma_smem(NT, sub, L.group, CPC) > kSmemPerCta) sub = (sub + 1) / 2;
+  const size_t smem = mma_smem(NT, sub, L.group, CPC);
   if (smem > 227 * 1024) return cudaErrorNotSupported;
   MmaParams p;
   p.vals = a.vals;
@@ -406,16 +458,17 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
   p.split_chunks = split_chunks;
   p.nsplit = nsplit;
   p.sub_chunks = sub;
-  p.sub_groups = (sub * 64 + L.group - 1) / L.group + 1;
+  p.sub_groups = (sub * CPC + L.group - 1) / L.group + 1;
+  p.ngroups = (int)L.ngroups;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_mma24<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_mma24<NT, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
     if (e != cudaSuccess) return e;
     if (kMaxSplit > 8) {
-      e = cudaFuncSetAttribute(k_mma24<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(k_mma24<NT, N>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
     }
     attr_set[dev] = true;
@@ -434,7 +487,7 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = SGEMV_MMA_PDL ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_mma24<NT>, p);
+  return cudaLaunchKernelEx(&cfg, k_mma24<NT, N>, p);
 }
 
 int g_sms[64] = {0};
@@ -442,7 +495,7 @@ int g_sms[64] = {0};
 }  // namespace
 
 cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s) {
-  if (L.n_keep != 2 || a.m < 2 || a.m > 64 || L.rows == 0 || L.cols == 0)
+  if (a.m < 2 || a.m > 64 || L.rows == 0 || L.cols == 0)
     return cudaErrorNotSupported;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
@@ -453,15 +506,28 @@ cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s) {
     g_sms[dev] = n;
   }
   const int nt = (a.m + 7) / 8;
+  const int sms = g_sms[dev];
+  if (L.n_keep == 2) {
+    switch (nt) {
+      case 1: return launch_nt<1, 2>(L, a, s, sms);
+      case 2: return launch_nt<2, 2>(L, a, s, sms);
+      case 3: return launch_nt<3, 2>(L, a, s, sms);
+      case 4: return launch_nt<4, 2>(L, a, s, sms);
+      case 5: return launch_nt<5, 2>(L, a, s, sms);
+      case 6: return launch_nt<6, 2>(L, a, s, sms);
+      case 7: return launch_nt<7, 2>(L, a, s, sms);
+      default: return launch_nt<8, 2>(L, a, s, sms);
+    }
+  }
   switch (nt) {
-    case 1: return launch_nt<1>(L, a, s, g_sms[dev]);
-    case 2: return launch_nt<2>(L, a, s, g_sms[dev]);
-    case 3: return launch_nt<3>(L, a, s, g_sms[dev]);
-    case 4: return launch_nt<4>(L, a, s, g_sms[dev]);
-    case 5: return launch_nt<5>(L, a, s, g_sms[dev]);
-    case 6: return launch_nt<6>(L, a, s, g_sms[dev]);
-    case 7: return launch_nt<7>(L, a, s, g_sms[dev]);
-    default: return launch_nt<8>(L, a, s, g_sms[dev]);
+    case 1: return launch_nt<1, 1>(L, a, s, sms);
+    case 2: return launch_nt<2, 1>(L, a, s, sms);
+    case 3: return launch_nt<3, 1>(L, a, s, sms);
+    case 4: return launch_nt<4, 1>(L, a, s, sms);
+    case 5: return launch_nt<5, 1>(L, a, s, sms);
+    case 6: return launch_nt<6, 1>(L, a, s, sms);
+    case 7: return launch_nt<7, 1>(L, a, s, sms);
+    default: return launch_nt<8, 1>(L, a, s, sms);
   }
 }
 
