@@ -104,3 +104,20 @@ def test_pack_scored_rejects_bad_inputs(native):
     with pytest.raises(SgemvError) as e:
         h.run(x, y)
     assert e.value.code == native.SGEMV_ERR_STATE
+
+
+def test_pack_scored_with_row_groups(native, orc):
+    """Eq. 3 pruning on a handle with a group size per row: the oracle's
+    scored pruning, then its per-row quantisation and encoding."""
+    rows, cols = 90, 1024
+    W, xnorm, grad = _inputs(12, rows, cols)
+    rg = np.random.default_rng(13).choice([64, 128, 256], rows).astype(np.int32)
+    for n_keep in (1, 2):
+        pos = orc.prune_scored(W, xnorm, grad, n_keep)
+        q, sc, z = orc.quantize_rowg(W, pos, n_keep, rg)
+        vals, idx = orc.encode(pos, q, rows, cols, n_keep)
+        h = native.SparseGemv(rows, cols, n_keep, None, row_group=rg)
+        h.pack_scored(W, xnorm, grad)
+        ev, ei, es, ez = h.export_canonical()
+        assert np.array_equal(ev, vals) and np.array_equal(ei, idx)
+        assert np.array_equal(es, sc) and np.array_equal(ez, z)
