@@ -481,7 +481,9 @@ def run_ours(args, rank, world, local):
     batch = None
     batch_mixed = None
     rowg = None
+    sweep = None
     if not args.no_batch:
+        sweep = run_gemv_sweep(args, swo, dev, stream, l2, read_peak()[0])
         batch = run_batch_sweep(args, swo, dev, stream, l2)
         # the same verification batches on the mixed (N, g) layer set
         batch_mixed = run_batch_sweep(args, swo, dev, stream, l2, gvs, (4, 16, 64))
@@ -563,6 +565,7 @@ def run_ours(args, rank, world, local):
         "batch_m": batch,
         "batch_m_layerset": batch_mixed,
         "row_groups": rowg,
+        "gemv_sweep": sweep,
         "copies_identical_y": same,
         "launch_mode": ("grouped calls: run_group(q,k,v), run(o), run_group(gate,up), "
                         "run(down)" if grouped else "per-matrix calls"),
@@ -634,6 +637,75 @@ def run_batch_sweep(args, swo, dev, stream, l2, gvs=None, ms=None):
     for st in sets:
         for h in st:
             h.close()
+    return out
+
+
+def run_gemv_sweep(args, swo, dev, stream, l2, peak):
+    """M = 1, one GEMV at a time, for the single-layer workloads (4096x4096
+    2:4 g128; 4096x4096 with outliers at 1:4 g256 and 2:4 g64) and the large
+    layers (8192x8192, 28672x8192, 8192x28672, g128): us per call, GB/s,
+    fraction of the HBM peak, and cuBLAS dense binary16 on the same shape."""
+    import torch
+    sptr = stream.cuda_stream
+    out = []
+    for gv in synth.config1(args.seed) + synth.config2(args.seed) + synth.config5(args.seed):
+        W = gv.weight()
+        h0 = swo.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group, device=dev.index)
+        h0.pack(W)
+        del W
+        canon = h0.export_canonical()
+        pb = gv.packed_bytes()
+        copies = max(2, math.ceil(4 * l2 / pb) + 1)
+        hs = [h0]
+        for _ in range(copies - 1):
+            h = swo.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group, device=dev.index)
+            h.import_canonical(*canon)
+            hs.append(h)
+        del canon
+        x = torch.from_numpy(gv.x(1)).to(dev)
+        y = torch.empty((1, gv.rows), dtype=torch.float16, device=dev)
+
+        def timed(fn, reps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                fn(0)
+                with torch.cuda.graph(g, stream=stream):
+                    for k in range(reps):
+                        fn(k)
+            g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(5):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / (5 * reps)
+
+        us = timed(lambda k: hs[k % copies].run(x, y, sptr), 4 * copies)
+        for h in hs:
+            h.close()
+        del hs
+        dense = None
+        try:
+            db = 2 * gv.rows * gv.cols
+            dc = max(2, math.ceil(4 * l2 / db) + 1)
+            dws = [torch.randn(gv.rows, gv.cols, device=dev, dtype=torch.float16)
+                   for _ in range(dc)]
+            dense = timed(lambda k: torch.matmul(x, dws[k % dc].t(), out=y), 2 * dc)
+            del dws
+        except Exception:  # pragma: no cover - reported as missing
+            dense = None
+        b = gv.bytes(1)
+        out.append({"name": gv.name, "shape": [gv.rows, gv.cols],
+                    "n_keep": gv.n_keep, "group": gv.group, "bytes": b,
+                    "us": round(us, 3), "gbs": round(b / us / 1e3, 1),
+                    "frac_of_peak": round(b / us / 1e3 / peak, 3),
+                    "dense_fp16_us": round(dense, 3) if dense else None,
+                    "speedup_vs_dense_fp16": round(dense / us, 2) if dense else None})
+        torch.cuda.empty_cache()
     return out
 
 

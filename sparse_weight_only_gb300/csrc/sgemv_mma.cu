@@ -27,10 +27,13 @@
 //    the buffer (conflict-free).
 //  * scale: each k-tile lies inside one group; the MMA accumulates a group
 //    into a temporary that is scaled by s and added in fp32.
-//  * split-K across the CTAs of a thread-block cluster: every CTA writes its
-//    fp32 partial tile to its own shared memory and the cluster reduces the
-//    tile through distributed shared memory in rank order -- deterministic,
-//    no global scratch.
+//  * split-K across the CTAs of a thread-block cluster, reduced through
+//    distributed shared memory in rank order -- deterministic, no global
+//    scratch.  Up to two n-tiles (m <= 16) every CTA pushes its partial rows
+//    to their owner rank with remote stores counted on the owner's mbarrier
+//    (one split cluster barrier, arrive at launch and wait after the main
+//    loop, orders the setup); wider tiles are written to each CTA's shared
+//    memory and pulled by the owners between two cluster barriers.
 #include <cooperative_groups.h>
 
 #include "sgemv_internal.cuh"
@@ -64,6 +67,7 @@ struct MmaParams {
   int sub_chunks;     // chunks of weights and x staged at a time
   int sub_groups;     // scale/zero words per row staged per sub-slice (bound)
   int ngroups;        // scale/zero groups per row
+  int* err;           // device error word (a bounded wait that gave up)
 };
 
 // half2 (q_a - z, q_b - z) of the quad whose byte is byte `t` of `w`.
@@ -123,6 +127,59 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
+}
+
+// ---- cluster reduction primitives: an mbarrier counting the bytes that the
+// other ranks push, their remote stores, and the split cluster barrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+      "f"(a), "f"(b), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void sts_v2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// A wait gives up after this long (ns): far beyond any legitimate stall.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+// The split-K partials travel by remote stores from the accumulators (one
+// 8-byte store per row pair and n-tile, counted on the owner's mbarrier) for
+// up to two n-tiles; wider tiles write them to shared memory and the owners
+// pull them after a cluster barrier, which costs less than thousands of small
+// remote stores per CTA.
+__host__ __device__ constexpr bool push_reduce(int nt) { return nt <= 2; }
+
+// Rows of the CTA tile that cluster rank q reduces: [q R / n, (q + 1) R / n).
+__device__ __forceinline__ int owner_rank(int r, int nsplit) {
+  return ((r + 1) * nsplit - 1) / kRowsCta;
 }
 
 // 1:4 operand of quads t and t + 4 of k-step kt for one row, as two half2
@@ -235,7 +292,13 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(xs);
   const int xs_bytes = (mp * xs_stride * 2 + 127) & ~127;
   const uint32_t wbuf0 = xs_s + (uint32_t)xs_bytes;
-  float* part = reinterpret_cast<float*>(smem);
+  // after them: the receive buffer of the split-K reduction (one slot of
+  // ceil(R / nsplit) rows x mp per rank) and its mbarrier
+  float* part = reinterpret_cast<float*>(smem);   // pull reduction: reuses the front
+  const int rq = (kRowsCta + p.nsplit - 1) / p.nsplit;
+  const uint32_t recv_s = wbuf0 + (uint32_t)(2 * W.bytes);
+  const uint32_t rbar = recv_s + (uint32_t)(p.nsplit * rq * mp * 4);
+  const float* recv = reinterpret_cast<const float*>(smem + (recv_s - xs_s));
 
   const int row0 = (blockIdx.x / p.nsplit) * kRowsCta;
   const int rowbase = row0 + warp * 16;
@@ -263,6 +326,19 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
 
   // ldmatrix row address of this thread: matrix j = lane / 8, row lane % 8
   const uint32_t ld_base = xs_s + (uint32_t)(((lane & 7) * xs_stride + (lane >> 3) * 8) * 2);
+
+  // this rank's rows of the reduction; the bytes the other ranks will push
+  const int r_lo = rank * kRowsCta / p.nsplit, r_hi = (rank + 1) * kRowsCta / p.nsplit;
+  if constexpr (push_reduce(NT)) {
+    if (threadIdx.x == 0) {
+      mbar_init(rbar, 1);
+      mbar_arrive_expect_tx(rbar, (uint32_t)((p.nsplit - 1) * (r_hi - r_lo) * mp * 4));
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // first half of a cluster barrier: every rank's receive side is set up
+    // before any rank pushes (the wait comes after the main loop)
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  }
 
   // weights of the first sub-slice: in flight while x is staged
   if (nsub > 0) {
@@ -378,50 +454,97 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
     }
   }
   cp_wait<0>();
-  __syncthreads();  // every warp is done with x and the buffers: part reuses them
 
-  // ---- split-K reduction across the cluster (rank order, deterministic)
-  // part: [kRowsCta][mp] fp32 of this CTA
+  if constexpr (!push_reduce(NT)) {
+    // ---- split-K reduction across the cluster, pulled (rank order,
+    // deterministic): every CTA writes its fp32 partial tile to its own
+    // shared memory; each rank reads its rows from all ranks
+    __syncthreads();  // every warp is done with x and the buffers: part reuses them
 #pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    const int mc = n * 8 + 2 * t;
-    part[lr_g * mp + mc] = acc[n][0];
-    part[lr_g * mp + mc + 1] = acc[n][1];
-    part[lr_g8 * mp + mc] = acc[n][2];
-    part[lr_g8 * mp + mc + 1] = acc[n][3];
+    for (int n = 0; n < NT; ++n) {
+      const int mc = n * 8 + 2 * t;
+      part[lr_g * mp + mc] = acc[n][0];
+      part[lr_g * mp + mc + 1] = acc[n][1];
+      part[lr_g8 * mp + mc] = acc[n][2];
+      part[lr_g8 * mp + mc + 1] = acc[n][3];
+    }
+    cluster.sync();
+    {
+      const int n_el = (r_hi - r_lo) * p.m;
+      const float* rp[kMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kMaxSplit; ++q)
+        rp[q] = cluster.map_shared_rank(part, q < p.nsplit ? q : 0);
+      for (int e = threadIdx.x; e < n_el; e += kW * 32) {
+        const int lr = r_lo + e / p.m, mm = e % p.m;
+        float v[kMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q) v[q] = q < p.nsplit ? rp[q][lr * mp + mm] : 0.0f;
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q) sum += v[q];
+        const int row = row0 + lr;
+        if (row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(sum);
+      }
+    }
+    cluster.sync();  // no CTA leaves while its partial tile is being read
+    return;
   }
-  cluster.sync();
-  {
-    // rank k finishes rows [k * kRowsCta / nsplit, (k+1) * kRowsCta / nsplit)
-    const int r_lo = rank * kRowsCta / p.nsplit, r_hi = (rank + 1) * kRowsCta / p.nsplit;
-    const int n_el = (r_hi - r_lo) * p.m;
-    const float* rp[kMaxSplit];
+
+  // ---- split-K reduction across the cluster, pushed (rank order,
+  // deterministic): every rank sends its partial rows to the rank that owns
+  // them straight from the accumulators (remote stores counted on the
+  // owner's mbarrier); an owner sums the nsplit slots of its rows in rank
+  // order
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 #pragma unroll
-    for (int q = 0; q < kMaxSplit; ++q)
-      rp[q] = cluster.map_shared_rank(part, q < p.nsplit ? q : 0);
-    for (int e = threadIdx.x; e < n_el; e += kW * 32) {
-      const int lr = r_lo + e / p.m, mm = e % p.m;
-      float v[kMaxSplit];
+  for (int h = 0; h < 2; ++h) {
+    const int r = h ? lr_g8 : lr_g;
+    const int q = owner_rank(r, p.nsplit);
+    const int rl = r - q * kRowsCta / p.nsplit;
 #pragma unroll
-      for (int q = 0; q < kMaxSplit; ++q) v[q] = q < p.nsplit ? rp[q][lr * mp + mm] : 0.0f;
-      float sum = 0.0f;
-#pragma unroll
-      for (int q = 0; q < kMaxSplit; ++q) sum += v[q];
-      const int row = row0 + lr;
-      if (row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(sum);
+    for (int n = 0; n < NT; ++n) {
+      const uint32_t off = (uint32_t)(((rank * rq + rl) * mp + n * 8 + 2 * t) * 4);
+      const float a = acc[n][2 * h], b = acc[n][2 * h + 1];
+      if (q == rank)
+        sts_v2(recv_s + off, a, b);
+      else
+        st_async_v2(map_rank(recv_s + off, q), a, b, map_rank(rbar, q));
     }
   }
-  cluster.sync();  // no CTA leaves while its partial tile is being read
+  __syncthreads();  // this rank's own slot is in place
+  bool ok = mbar_try_wait(rbar, 0);
+  if (!ok) {
+    const unsigned long long t0 = global_ns();
+    while (!(ok = mbar_try_wait(rbar, 0)))
+      if (global_ns() - t0 > kWaitLimitNs) break;
+    if (!ok) {
+      if (threadIdx.x == 0) atomicCAS(p.err, 0, kDevErrTimeout);
+      return;
+    }
+  }
+  const int n_el = (r_hi - r_lo) * p.m;
+  for (int e = threadIdx.x; e < n_el; e += kW * 32) {
+    const int rl = e / p.m, mm = e % p.m;
+    float sum = 0.0f;
+    for (int q = 0; q < p.nsplit; ++q) sum += recv[(q * rq + rl) * mp + mm];
+    const int row = row0 + r_lo + rl;
+    if (row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(sum);
+  }
 }
 
 // Shared memory of a launch with sub-slices of `sc` chunks of `cpc` columns.
-size_t mma_smem(int nt, int sc, int group, int cpc) {
+size_t mma_smem(int nt, int sc, int group, int cpc, int nsplit) {
   const int mp = nt * 8;
   const WGeom W(sc, (sc * cpc + group - 1) / group + 1);
   const size_t xs = ((size_t)mp * (sc * cpc + 8) * 2 + 127) & ~(size_t)127;
   const size_t main = xs + 2 * (size_t)W.bytes;
-  const size_t red = (size_t)kRowsCta * mp * 4;
-  return main > red ? main : red;
+  if (!push_reduce(nt)) {
+    const size_t red = (size_t)kRowsCta * mp * 4;
+    return main > red ? main : red;
+  }
+  const size_t recv = (size_t)nsplit * ((kRowsCta + nsplit - 1) / nsplit) * mp * 4;
+  return main + recv + 16;
 }
 
 template <int NT, int N>
@@ -439,8 +562,8 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
   nsplit = (chunks + split_chunks - 1) / split_chunks;
   // sub-slices: as many chunks as fit two CTAs per SM
   int sub = min(split_chunks, 64);
-  while (sub > 1 && mma_smem(NT, sub, L.group, CPC) > kSmemPerCta) sub = (sub + 1) / 2;
-  const size_t smem = mma_smem(NT, sub, L.group, CPC);
+  while (sub > 1 && mma_smem(NT, sub, L.group, CPC, nsplit) > kSmemPerCta) sub = (sub + 1) / 2;
+  const size_t smem = mma_smem(NT, sub, L.group, CPC, nsplit);
   if (smem > 227 * 1024) return cudaErrorNotSupported;
   MmaParams p;
   p.vals = a.vals;
@@ -460,6 +583,7 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
   p.sub_chunks = sub;
   p.sub_groups = (sub * CPC + L.group - 1) / L.group + 1;
   p.ngroups = (int)L.ngroups;
+  p.err = a.err;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
