@@ -482,8 +482,9 @@ def run_ours(args, rank, world, local):
     batch_mixed = None
     rowg = None
     sweep = None
-    if not args.no_batch:
+    if not args.no_batch and not args.no_sweep:
         sweep = run_gemv_sweep(args, swo, dev, stream, l2, read_peak()[0])
+    if not args.no_batch:
         batch = run_batch_sweep(args, swo, dev, stream, l2)
         # the same verification batches on the mixed (N, g) layer set
         batch_mixed = run_batch_sweep(args, swo, dev, stream, l2, gvs, (4, 16, 64))
@@ -770,6 +771,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ungrouped", action="store_true",
                     help="time one call per matrix instead of the grouped calls")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the one-GEMV-at-a-time sweep over the single and large layers")
     ap.add_argument("--no-batch", action="store_true",
                     help="skip the small-M (config 4) sweep")
     args = ap.parse_args(argv)
