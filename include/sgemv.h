@@ -183,9 +183,11 @@ int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
  *             n_keep and group may differ;
  *   x_dev   : m x cols binary16, 16-byte aligned, shared by all;
  *   y_devs  : count device pointers, y_devs[i] is m x rows_i binary16,
- *             2-byte aligned, none overlapping x_dev;
+ *             2-byte aligned, none overlapping x_dev or one another
+ *             (SGEMV_ERR_ARG otherwise);
  *   m       : 0 <= m <= every handle's max_m.
- * Asynchronous on `stream`, like sgemv_run; count = 0 is a no-op.
+ * Asynchronous on `stream`, like sgemv_run; count = 0 is a no-op.  The
+ * next work on the stream sees every y_i complete.
  */
 int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
                     void* const* y_devs, int m, void* stream);

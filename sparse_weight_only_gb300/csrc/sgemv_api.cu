@@ -493,6 +493,17 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
         return fail(SGEMV_ERR_ARG, "x and y_devs[%d] overlap", i);
     }
   }
+  // outputs must be disjoint (each is written by a different launch part)
+  if (m > 0)
+    for (int i = 0; i < count; ++i)
+      for (int j = i + 1; j < count; ++j) {
+        const char* a = static_cast<const char*>(y_devs[i]);
+        const char* b = static_cast<const char*>(y_devs[j]);
+        const size_t an = (size_t)m * handles[i]->L.rows * 2;
+        const size_t bn = (size_t)m * handles[j]->L.rows * 2;
+        if (a && b && an && bn && a < b + bn && b < a + an)
+          return fail(SGEMV_ERR_ARG, "y_devs[%d] and y_devs[%d] overlap", i, j);
+      }
   if (x_dev && ((uintptr_t)x_dev & 15u))
     return fail(SGEMV_ERR_ARG, "x_dev must be 16-byte aligned");
   DeviceGuard g(handles[0]->device);

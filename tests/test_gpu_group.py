@@ -98,3 +98,36 @@ def test_group_edges(native, orc):
                                                     device="cuda"),
                          [torch.empty((2, 40), dtype=torch.float16, device="cuda")])
     assert e.value.code == native.SGEMV_ERR_ARG
+
+
+def test_group_outputs_complete_for_next_work(native, orc):
+    """Work queued right after a grouped call on the same stream (no host
+    synchronisation in between) sees every output of both launches (one per
+    N) complete."""
+    cols = 4096
+    specs = [(4096, 1, 256), (4096, 2, 128), (4096, 1, 128)]   # q, k, v shapes
+    mats = _mats(native, orc, specs, cols)
+    x = torch.from_numpy(synth.activations(5, 1, cols)).cuda()
+    singles = []
+    for h, _ in mats:
+        y = torch.empty((1, h.rows), dtype=torch.float16, device="cuda")
+        h.run(x, y)
+        singles.append(y)
+    torch.cuda.synchronize()
+    want = torch.cat(singles, dim=1)
+    stream = torch.cuda.current_stream()
+    for rep in range(20):
+        ys = _ys(mats, 1)
+        native.run_group([h for h, _ in mats], x, ys, stream.cuda_stream)
+        got = torch.cat(ys, dim=1)          # queued on the same stream
+        torch.cuda.synchronize()
+        assert torch.equal(got, want), f"repetition {rep}"
+
+
+def test_group_rejects_overlapping_outputs(native, orc):
+    cols = 256
+    mats = _mats(native, orc, [(64, 2, 64), (64, 1, 64)], cols)
+    x = torch.from_numpy(synth.activations(6, 1, cols)).cuda()
+    buf = torch.empty((1, 96), dtype=torch.float16, device="cuda")
+    with pytest.raises(native.SgemvError):
+        native.run_group([h for h, _ in mats], x, [buf[:, :64], buf[:, 32:96]])

@@ -119,7 +119,7 @@ def test_run_parity_small(native, orc, rows, cols, n_keep, group, dist, m):
             f"{rows}x{cols} N={n_keep} g={group} m={m}")
 
 
-@pytest.mark.parametrize("m", [1, 2, 4, 16, 33, 64])
+@pytest.mark.parametrize("m", [1, 2, 4, 9, 16, 17, 24, 33, 64])
 def test_run_parity_all_m(native, orc, m):
     rows, cols = 200, 1536
     for n_keep, group in ((2, 128), (1, 64)):
