@@ -230,6 +230,40 @@ def oracle_time(packed, budget_s: float, min_rows: int = 1):
     return total_b, total_t, rows_done
 
 
+def oracle_time_threads(packed, budget_s: float, threads: int):
+    """The same row blocks as oracle_time, spread over `threads` host threads
+    (the oracle's C matvec runs without the interpreter lock), in whole passes
+    over the matrices until `budget_s` of wall time has elapsed.  Returns
+    (bytes, seconds, rows_done)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    tasks = []
+    for gv, p, x in packed:
+        nr = max(1, gv.rows // 64)
+        for start in range(0, gv.rows - nr + 1, nr):
+            tasks.append((gv, p, x, start, nr))
+    # interleave the matrices so that any prefix samples all of them
+    tasks.sort(key=lambda t: (t[3] // t[4], t[0].name))
+    t0 = time.perf_counter()
+
+    def one(task):
+        gv, p, x, start, nr = task
+        if time.perf_counter() - t0 >= budget_s:
+            return 0.0, 0
+        oracle.matvec(p, x, np.arange(start, start + nr, dtype=np.int64))
+        return nr / gv.rows * gv.packed_bytes() + 2 * gv.cols + 2 * nr, nr
+
+    total_b, total_r = 0.0, 0
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:   # whole passes over the layer set until the budget is spent
+            done = list(ex.map(one, tasks))
+            total_b += sum(d[0] for d in done)
+            total_r += sum(d[1] for d in done)
+            if time.perf_counter() - t0 >= budget_s:
+                break
+    return total_b, time.perf_counter() - t0, total_r
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -515,6 +549,8 @@ def run_ours(args, rank, world, local):
 
     # CPU oracle on the host cores (rank 0 only), ~10 s bounded sample
     cpu = None
+    cpu_all = None
+    oracle_pack = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
@@ -527,6 +563,20 @@ def run_ours(args, rank, world, local):
         cpu = {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{rows} rows of the layer set in blocks of 1/64 of a "
                          f"matrix, {t:.1f} s single-threaded"}
+        threads = os.cpu_count() or 1
+        b, t, rows = oracle_time_threads(packed, args.cpu_seconds, threads)
+        cpu_all = {"value": b / t / 1e9, "unit": "GB/s", "cores": threads,
+                   "kind": "oracle, row blocks on a thread pool",
+                   "sample": f"{rows} rows of the layer set in blocks of 1/64 of a "
+                             f"matrix, {t:.1f} s wall on {threads} threads"}
+        # the oracle's pack (prune, quantise, encode) of one matrix, timed apart
+        gk = next(g for g in gvs if g.name == "k")
+        Wk = gk.weight()
+        t0 = time.perf_counter()
+        oracle.pack(Wk, gk.n_keep, gk.group)
+        oracle_pack = {"matrix": f"k {gk.rows}x{gk.cols} {gk.n_keep}:4 g{gk.group}",
+                       "seconds": round(time.perf_counter() - t0, 3), "cores": 1}
+        del Wk
 
     peak, peak_src = read_peak()
     traffic = read_traffic("sgemv_layerset_m1")
@@ -556,6 +606,8 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": sum(2 * m * g.rows for g in gvs),
                 "api": "sgemv_run_host per matrix + stream sync per step"},
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
+        "oracle_pack": oracle_pack,
         "clocks": clocks.summary(),
         "gpu_launches": launches,
         "per_matrix": per,
@@ -675,15 +727,16 @@ def run_gemv_sweep(args, swo, dev, stream, l2, peak):
                         fn(k)
             g.replay()
             torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
+            # median of 10 timed replays of the whole rotation
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(10)]
             with torch.cuda.stream(stream):
-                e0.record(stream)
-                for _ in range(5):
+                for a, b in ev:
+                    a.record(stream)
                     g.replay()
-                e1.record(stream)
+                    b.record(stream)
             torch.cuda.synchronize()
-            return e0.elapsed_time(e1) * 1e3 / (5 * reps)
+            return float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e3 / reps
 
         us = timed(lambda k: hs[k % copies].run(x, y, sptr), 4 * copies)
         for h in hs:
