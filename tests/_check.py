@@ -1,6 +1,6 @@
 """Tolerance check of a GPU y against the oracle.
 
-Spec bound: max |dy| <= 1e-2 * ||row||_1 * 2^-10 and rel-L2 <= 1e-3.
+The stated y tolerance: max |dy| <= 1e-2 * ||row||_1 * 2^-10 and rel-L2 <= 1e-3.
 Reading (the bound is silent on which norm and which reference): ||row||_1
 is the L1 norm of the dequantised pruned row, and the binary16 y is
 compared with binary16(y_ref), allowing the larger of that bound and one
