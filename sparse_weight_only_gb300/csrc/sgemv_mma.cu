@@ -286,15 +286,15 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   const int mp = NT * 8;                       // padded activation rows
   const int xs_stride = p.sub_chunks * CPC + 8; // halves per staged x row
   const WGeom W(p.sub_chunks, p.sub_groups);
-  // shared memory: x of the sub-slice | two weight buffers; after the main
-  // loop the partial tile for the cluster reduction reuses the front
+  // shared memory: x of the sub-slice | two weight buffers | (pushed
+  // reduction) the receive buffer, one slot of ceil(R / nsplit) rows x mp
+  // per rank, and its mbarrier.  The pulled reduction writes its partial
+  // tile over the front once the main loop is done.
   __half* xs = reinterpret_cast<__half*>(smem);
   const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(xs);
   const int xs_bytes = (mp * xs_stride * 2 + 127) & ~127;
   const uint32_t wbuf0 = xs_s + (uint32_t)xs_bytes;
-  // after them: the receive buffer of the split-K reduction (one slot of
-  // ceil(R / nsplit) rows x mp per rank) and its mbarrier
-  float* part = reinterpret_cast<float*>(smem);   // pull reduction: reuses the front
+  float* part = reinterpret_cast<float*>(smem);
   const int rq = (kRowsCta + p.nsplit - 1) / p.nsplit;
   const uint32_t recv_s = wbuf0 + (uint32_t)(2 * W.bytes);
   const uint32_t rbar = recv_s + (uint32_t)(p.nsplit * rq * mp * 4);
