@@ -193,7 +193,11 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
                     void* const* y_devs, int m, void* stream);
 
 /* Synchronise the device, then return and clear the handle's device error
- * word (SGEMV_OK if no kernel reported an error since the last call). */
+ * word (SGEMV_OK if no kernel reported an error since the last call).  A
+ * product kernel reports SGEMV_ERR_TIMEOUT when its one bounded wait -- the
+ * split-K reduction of the small-batch kernel (2 <= m <= 16) waiting for the
+ * other CTAs of its cluster -- gave up after about a second; the outputs of
+ * that call are then undefined. */
 int sgemv_status(sgemv_t h);
 
 /*
