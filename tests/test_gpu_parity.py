@@ -104,6 +104,21 @@ def test_pack_parity_special_groups(native, orc):
                            orc.pack(W, n_keep, 64))
 
 
+def test_pack_parity_ties_to_even(native, orc):
+    """Halfway quantiser cases (tests/_ties.py): the GPU packer's codes equal
+    the hand-derived ties-to-even table, and the oracle's bytes."""
+    import _ties
+    for n_keep in (1, 2):
+        for group in (64, 128):
+            W, _ = _ties.weight(n_keep, group)
+            h = _lib_pack(native, W, n_keep, group)
+            vals, idx, scale, zero = h.export_canonical()
+            ev, ei, es, ez = _ties.expected_bytes(n_keep, group)
+            assert np.array_equal(vals, ev) and np.array_equal(idx, ei)
+            assert np.array_equal(scale, es) and np.array_equal(zero, ez)
+            _assert_same_bytes(h, orc.pack(W, n_keep, group))
+
+
 @pytest.mark.parametrize("rows,cols,n_keep,group,dist", SMALL)
 @pytest.mark.parametrize("m", [1, 3, 8])
 def test_run_parity_small(native, orc, rows, cols, n_keep, group, dist, m):

@@ -417,6 +417,30 @@ def test_quant_bounds_random(orc):
         assert q.shape == (6, P)
 
 
+def test_quant_ties_to_even(orc):
+    """Halfway cases of z = rint(-lo / s) and q = rint(w / s) + z round to
+    even (section 3.2, FP16 -> INT4 group quantisation; the pages leave the
+    rounding of halves open and the IEEE default is read).  The codes are the
+    hand-derived table in tests/_ties.py, not the oracle's own output."""
+    import _ties
+    # the fixture discriminates: halves rounded away from zero give other codes
+    away = [int(np.sign(k2) * np.floor(abs(k2) + 0.5)) for _, k2, _ in _ties.KEPT]
+    assert away != [k for _, _, k in _ties.KEPT]
+    assert int(np.floor(4.5 + 0.5)) != _ties.Z
+    for n_keep in (1, 2):
+        for group in (64, 128):
+            W, kept = _ties.weight(n_keep, group)
+            p = orc.pack(W, n_keep, group)
+            vals, idx, scale, zero = _ties.expected_bytes(n_keep, group)
+            assert p.scale.tolist() == scale.tolist()
+            assert p.zero.tolist() == zero.tolist()
+            assert np.array_equal(p.vals, vals), (n_keep, group)
+            assert np.array_equal(p.idx, idx), (n_keep, group)
+            pos = orc.prune(W, n_keep)
+            q, _, _ = orc.quantize(W, pos, n_keep, group)
+            assert q[0].tolist() == _ties.codes(kept)
+
+
 def test_quant_special_groups(orc):
     # all-zero group: s = 1.0, z = 0, q = 0
     W = np.zeros((1, 64), np.float32)
