@@ -156,6 +156,9 @@ int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
  *   accumulation is fp32, each y element rounded once to binary16.
  * Asynchronous on `stream`: returns after the launch, reporting argument
  * and launch errors only.  The handle must have been packed or imported.
+ * cols = 0 writes y = +0.  A matrix whose device layout holds 2^31 or more
+ * 32-weight chunks or scale/zero words (48 GiB or more of packed weight)
+ * -> SGEMV_ERR_UNSUPPORTED.
  */
 int sgemv_run(sgemv_t h, const void* x_dev, void* y_dev, int m, void* stream);
 
@@ -196,9 +199,26 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
  * word (SGEMV_OK if no kernel reported an error since the last call).  A
  * product kernel reports SGEMV_ERR_TIMEOUT when its one bounded wait -- the
  * split-K reduction of the small-batch kernel (2 <= m <= 16) waiting for the
- * other CTAs of its cluster -- gave up after about a second; the outputs of
- * that call are then undefined. */
+ * partial sums of the other CTAs of its cluster -- gave up after about a
+ * second; the outputs of that call are then undefined.  What the limit
+ * guards against: a byte count the other CTAs can never reach (every CTA
+ * still issues all of its sends, and no CTA retires before every CTA of its
+ * cluster has issued them, so no late store lands in a retired CTA).  What
+ * it cannot guard against: a CTA of the cluster that never reaches its
+ * sends -- the launch then does not finish. */
 int sgemv_status(sgemv_t h);
+
+/*
+ * Failure-detection test hook (not a paper operation).  The next `runs`
+ * products on this handle that use the small-batch kernel's bounded wait
+ * (2 <= m <= 16, more than one CTA per row tile) withhold every cluster
+ * rank's partial sums and shorten the wait to about 20 microseconds, so the
+ * wait runs out: sgemv_status then returns SGEMV_ERR_TIMEOUT and y of those
+ * calls is undefined.  No remote store is in flight when the wait gives up
+ * and the device stays usable; later calls run normally.  runs = 0 cancels;
+ * runs < 0 -> SGEMV_ERR_ARG.
+ */
+int sgemv_debug_withhold(sgemv_t h, int runs);
 
 /*
  * Byte counts of the canonical arrays and of the device-resident packed

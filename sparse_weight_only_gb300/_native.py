@@ -42,6 +42,7 @@ SIGNATURES = {
     "sgemv_run_host": (_I, [_P, _P, _P, _I, _P]),
     "sgemv_run_group": (_I, [_P, _I, _P, _P, _I, _P]),
     "sgemv_status": (_I, [_P]),
+    "sgemv_debug_withhold": (_I, [_P, _I]),
     "sgemv_sizes": (_I, [_P, _PSZ, _PSZ, _PSZ, _PSZ]),
     "sgemv_packed_bytes": (_SZ, [_P]),
     "sgemv_last_error": (ctypes.c_char_p, []),
@@ -243,6 +244,12 @@ class SparseGemv:
 
     def status(self) -> int:
         return int(load().sgemv_status(self._h))
+
+    def debug_withhold(self, runs: int) -> None:
+        """Failure-detection test hook: the next `runs` small-batch products
+        make their bounded split-K wait run out (sgemv_status then reports
+        SGEMV_ERR_TIMEOUT)."""
+        _check(load().sgemv_debug_withhold(self._h, runs), "sgemv_debug_withhold")
 
 
 def run_group(mats, x, ys, stream=None) -> None:

@@ -2,7 +2,7 @@
 // include/sgemv.h): argument checks, handle and device-buffer management,
 // host<->device transfers, and kernel dispatch.  No arithmetic of the
 // method happens here; every step of pack and run executes in the CUDA
-// kernels of sgemv_format.cu, sgemv_generic.cu, sgemv_m1.cu and sgemv_mma.cu.
+// kernels of sgemv_format.cu, sgemv_m1.cu and sgemv_mma.cu.
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -87,7 +87,9 @@ int dev_err_to_status(int word) {
     case sgemv::kDevErrBadIndex:
       return fail(SGEMV_ERR_ARG, "2:4 positions must ascend strictly within a quad");
     case sgemv::kDevErrTimeout:
-      return fail(SGEMV_ERR_TIMEOUT, "a kernel's bounded wait for its weight copies gave up");
+      return fail(SGEMV_ERR_TIMEOUT,
+                  "a bounded device wait gave up: the split-K reduction of the small-batch "
+                  "kernel did not receive every cluster rank's partial sums in time");
     default:
       return fail(SGEMV_ERR_CUDA, "device error word %d", word);
   }
@@ -410,13 +412,23 @@ static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s)
   a.m = m;
   a.err = h->d_err;
   if (m == 0 || L.rows == 0) return SGEMV_OK;
+  if (h->withhold_runs > 0 && sgemv::withhold_applies(L, m)) {
+    a.withhold = 1;
+    --h->withhold_runs;
+  }
+  // cols = 0: every output is the empty sum, +0
+  if (L.cols == 0) {
+    CUDA_TRY(cudaMemsetAsync(a.y, 0, (size_t)m * L.rows * sizeof(__half), s), "zero y");
+    return SGEMV_OK;
+  }
   // m = 1: the CUDA-core table kernel; m >= 2: the sparse tensor-core kernel
-  // (1:4 as 2:4 with a zero partner per quad); anything they do not cover:
-  // the general kernel
+  // (1:4 as 2:4 with a zero partner per quad)
   cudaError_t e = m == 1 ? sgemv::launch_m1(L, a, s) : sgemv::launch_mma(L, a, s);
   if (e == cudaErrorNotSupported) {
     (void)cudaGetLastError();
-    e = sgemv::launch_generic(L, a, s);
+    return fail(SGEMV_ERR_UNSUPPORTED,
+                "a %d x %d matrix is beyond the product kernels' 32-bit chunk index space",
+                L.rows, L.cols);
   }
   if (e != cudaSuccess) return cuda_fail(e, "SparseGemv launch");
   return SGEMV_OK;
@@ -543,16 +555,21 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
         cudaError_t e = sgemv::launch_m1_group(Ls, as, k, s);
         if (e == cudaErrorNotSupported) {
           (void)cudaGetLastError();
-          for (int q = 0; q < k; ++q) {
-            e = sgemv::launch_generic(Ls[q], as[q], s);
-            if (e != cudaSuccess) break;
-          }
+          return fail(SGEMV_ERR_UNSUPPORTED,
+                      "a grouped matrix is beyond the product kernels' 32-bit chunk index space");
         }
         if (e != cudaSuccess) return cuda_fail(e, "grouped SparseGemv launch");
         k = 0;
       }
     }
   }
+  return SGEMV_OK;
+}
+
+int sgemv_debug_withhold(sgemv_t h, int runs) {
+  if (int rc = check_handle(h)) return rc;
+  if (runs < 0) return fail(SGEMV_ERR_ARG, "runs=%d is negative", runs);
+  h->withhold_runs = runs;
   return SGEMV_OK;
 }
 

@@ -63,6 +63,7 @@ struct sgemv_ctx {
   int* d_rowg;         // rows group sizes
   int64_t* d_goff;     // rows + 1 canonical scale/zero offsets
   int64_t canon_groups;  // canonical scale/zero entries of the whole matrix
+  int withhold_runs;     // failure-detection test hook: runs left to sabotage
 };
 
 namespace sgemv {
@@ -104,13 +105,16 @@ struct RunArgs {
   __half* y;
   int m;
   int* err;   // the handle's device error word
+  int withhold = 0;   // failure-detection test hook (see sgemv_debug_withhold)
 };
-cudaError_t launch_generic(const Layout& L, const RunArgs& a, cudaStream_t s);
 // Each returns cudaErrorNotSupported when it does not cover the case.
 cudaError_t launch_m1(const Layout& L, const RunArgs& a, cudaStream_t s);
 cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s);
 // m = 1 over several matrices sharing x, cols and N in one launch.
 cudaError_t launch_m1_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s);
 int max_group();
+// Whether a product of m rows on this layout runs a kernel with the bounded
+// split-K wait that the failure-detection hook can make run out.
+bool withhold_applies(const Layout& L, int m);
 
 }  // namespace sgemv

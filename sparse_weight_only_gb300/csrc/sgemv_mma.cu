@@ -68,6 +68,10 @@ struct MmaParams {
   int sub_groups;     // scale/zero words per row staged per sub-slice (bound)
   int ngroups;        // scale/zero groups per row
   int* err;           // device error word (a bounded wait that gave up)
+  // Failure-detection test hook (0 in normal use): every rank withholds its
+  // split-K partials, so each owner's bounded wait runs out after wait_ns.
+  int withhold;
+  unsigned long long wait_ns;   // the owner's wait limit
 };
 
 // half2 (q_a - z, q_b - z) of the quad whose byte is byte `t` of `w`.
@@ -169,6 +173,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 // A wait gives up after this long (ns): far beyond any legitimate stall.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// The limit under the failure-detection test hook (the bytes never come).
+constexpr unsigned long long kInjectWaitNs = 20000ull;
 
 // The split-K partials travel by remote stores from the accumulators (one
 // 8-byte store per row pair and n-tile, counted on the owner's mbarrier) for
@@ -508,28 +514,44 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
       const float a = acc[n][2 * h], b = acc[n][2 * h + 1];
       if (q == rank)
         sts_v2(recv_s + off, a, b);
-      else
+      else if (!p.withhold)
         st_async_v2(map_rank(recv_s + off, q), a, b, map_rank(rbar, q));
     }
   }
+  // second split cluster barrier: this rank's sends are issued; no CTA
+  // leaves before every rank has issued its own, so no remote store can
+  // target a CTA that has retired
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   __syncthreads();  // this rank's own slot is in place
+  // The owner's wait for the other ranks' bytes is bounded: with a byte
+  // count that can never be reached it records SGEMV_ERR_TIMEOUT and skips
+  // the sum instead of spinning forever.
   bool ok = mbar_try_wait(rbar, 0);
   if (!ok) {
     const unsigned long long t0 = global_ns();
     while (!(ok = mbar_try_wait(rbar, 0)))
-      if (global_ns() - t0 > kWaitLimitNs) break;
-    if (!ok) {
-      if (threadIdx.x == 0) atomicCAS(p.err, 0, kDevErrTimeout);
-      return;
-    }
+      if (global_ns() - t0 > p.wait_ns) break;
   }
-  const int n_el = (r_hi - r_lo) * p.m;
-  for (int e = threadIdx.x; e < n_el; e += kW * 32) {
-    const int rl = e / p.m, mm = e % p.m;
-    float sum = 0.0f;
-    for (int q = 0; q < p.nsplit; ++q) sum += recv[(q * rq + rl) * mp + mm];
-    const int row = row0 + r_lo + rl;
-    if (row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(sum);
+  const bool timed_out = __syncthreads_or(!ok) != 0;   // one decision per CTA
+  if (!timed_out) {
+    const int n_el = (r_hi - r_lo) * p.m;
+    for (int e = threadIdx.x; e < n_el; e += kW * 32) {
+      const int rl = e / p.m, mm = e % p.m;
+      float sum = 0.0f;
+      for (int q = 0; q < p.nsplit; ++q) sum += recv[(q * rq + rl) * mp + mm];
+      const int row = row0 + r_lo + rl;
+      if (row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(sum);
+    }
+  } else if (threadIdx.x == 0) {
+    atomicCAS(p.err, 0, kDevErrTimeout);
+  }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (timed_out) {
+    // every rank's sends are issued by now: give stores still in flight a
+    // bounded time to land before this CTA's shared memory is released
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(rbar, 0))
+      if (global_ns() - t0 > p.wait_ns) break;
   }
 }
 
@@ -584,6 +606,8 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
   p.sub_groups = (sub * CPC + L.group - 1) / L.group + 1;
   p.ngroups = (int)L.ngroups;
   p.err = a.err;
+  p.withhold = a.withhold;
+  p.wait_ns = a.withhold ? kInjectWaitNs : kWaitLimitNs;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -617,6 +641,10 @@ cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms
 int g_sms[64] = {0};
 
 }  // namespace
+
+bool withhold_applies(const Layout& L, int m) {
+  return m >= 2 && push_reduce((m + 7) / 8) && L.rows > 0 && L.cols > 0;
+}
 
 cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s) {
   if (a.m < 2 || a.m > 64 || L.rows == 0 || L.cols == 0)
