@@ -45,9 +45,12 @@
  *     the end of the call's work;
  *   - a stream argument is a cudaStream_t passed as void*; NULL means the
  *     legacy default stream;
- *   - a handle is not safe for concurrent pack/import/export/destroy; any
- *     number of sgemv_run calls may run concurrently on different streams
- *     (they only read the packed weight).
+ *   - a handle is not safe for concurrent pack/import/export/destroy.
+ *     Products with m = 1 only read the packed weight, so any number of them
+ *     may run concurrently on different streams.  Products with m >= 2 also
+ *     use the handle's split-K workspace (partial tiles and per-tile
+ *     counters): such calls on one handle must not overlap on the GPU --
+ *     order them on one stream; calls on different handles are independent.
  */
 #ifndef SGEMV_H
 #define SGEMV_H
@@ -149,7 +152,11 @@ int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
                  uint16_t* zero);
 
 /*
- * y = W_hat . x for m activation rows (0 <= m <= max_m):
+ * y = W_hat . x for m activation rows (0 <= m <= max_m).  m = 1 runs the
+ * CUDA-core decode kernel; 2 <= m <= 64 (beam candidates, prefix-tree
+ * verification nodes: the paper's parallel verification, section 3.1) runs
+ * the sparse tensor-core kernel, with the 2-bit positions as the MMA's 2:4
+ * metadata and the accumulators in tensor memory.
  *   x_dev : m x cols binary16, row-major, 16-byte aligned, device memory;
  *   y_dev : m x rows binary16, row-major, 2-byte aligned, device memory,
  *           fully overwritten; must not overlap x_dev;
@@ -196,27 +203,23 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
                     void* const* y_devs, int m, void* stream);
 
 /* Synchronise the device, then return and clear the handle's device error
- * word (SGEMV_OK if no kernel reported an error since the last call).  A
- * product kernel reports SGEMV_ERR_TIMEOUT when its one bounded wait -- the
- * split-K reduction of the small-batch kernel (2 <= m <= 16) waiting for the
- * partial sums of the other CTAs of its cluster -- gave up after about a
- * second; the outputs of that call are then undefined.  What the limit
- * guards against: a byte count the other CTAs can never reach (every CTA
- * still issues all of its sends, and no CTA retires before every CTA of its
- * cluster has issued them, so no late store lands in a retired CTA).  What
- * it cannot guard against: a CTA of the cluster that never reaches its
- * sends -- the launch then does not finish. */
+ * word (SGEMV_OK if no kernel reported an error since the last call).  The
+ * batch kernel (2 <= m <= 64) reports SGEMV_ERR_TIMEOUT when one of its
+ * bounded waits -- for its own TMA copies and MMAs -- gave up after about a
+ * second: it then stops issuing work, lets the copies it issued land, frees
+ * its tensor memory, returns the split-K counters to zero and exits; the
+ * outputs of that call are undefined and later calls are unaffected.  No
+ * kernel of the library waits on another CTA. */
 int sgemv_status(sgemv_t h);
 
 /*
  * Failure-detection test hook (not a paper operation).  The next `runs`
- * products on this handle that use the small-batch kernel's bounded wait
- * (2 <= m <= 16, more than one CTA per row tile) withhold every cluster
- * rank's partial sums and shorten the wait to about 20 microseconds, so the
- * wait runs out: sgemv_status then returns SGEMV_ERR_TIMEOUT and y of those
- * calls is undefined.  No remote store is in flight when the wait gives up
- * and the device stays usable; later calls run normally.  runs = 0 cancels;
- * runs < 0 -> SGEMV_ERR_ARG.
+ * batch products on this handle (2 <= m <= 64) withhold their x copies and
+ * shorten the bounded waits to about 20 microseconds, so the wait for x runs
+ * out: sgemv_status then returns SGEMV_ERR_TIMEOUT and y of those calls is
+ * undefined.  Nothing the kernel waits for is in flight when it gives up,
+ * the device stays usable and later calls run normally.  m = 1 calls do not
+ * consume the hook.  runs = 0 cancels; runs < 0 -> SGEMV_ERR_ARG.
  */
 int sgemv_debug_withhold(sgemv_t h, int runs);
 

@@ -88,8 +88,8 @@ int dev_err_to_status(int word) {
       return fail(SGEMV_ERR_ARG, "2:4 positions must ascend strictly within a quad");
     case sgemv::kDevErrTimeout:
       return fail(SGEMV_ERR_TIMEOUT,
-                  "a bounded device wait gave up: the split-K reduction of the small-batch "
-                  "kernel did not receive every cluster rank's partial sums in time");
+                  "a bounded device wait gave up: a batch kernel's copies, MMAs or split-K "
+                  "partial sums did not arrive in time; the outputs of that call are undefined");
     default:
       return fail(SGEMV_ERR_CUDA, "device error word %d", word);
   }
@@ -126,6 +126,8 @@ void free_ctx(sgemv_t h) {
   cudaFree(h->d_err);
   cudaFree(h->d_rowg);
   cudaFree(h->d_goff);
+  cudaFree(h->tc.scratch);
+  cudaFree(h->tc.counters);
   if (h->stream) cudaStreamDestroy(h->stream);
   delete h;
 }
@@ -232,6 +234,23 @@ static int create_impl(sgemv_t* out, int rows, int cols, int n_keep, int group,
       if (e != cudaSuccess) rc = cuda_fail(e, "copy row groups");
     }
     delete[] off;
+  }
+  if (!rc && max_m >= 2 && rows > 0 && cols > 0) {
+    // the tensor-core batch kernel: split-K workspace, zeroed per-tile
+    // arrival counters, and tensor maps of the packed weight
+    rc = try_alloc((void**)&h->tc.scratch, sgemv::tc_scratch_bytes(max_m),
+                   "cudaMalloc split-K workspace");
+    const size_t cnt = (size_t)sgemv::tc_tiles(h->L) * sizeof(int);
+    if (!rc) rc = try_alloc((void**)&h->tc.counters, cnt, "cudaMalloc split-K counters");
+    if (!rc) {
+      e = cudaMemset(h->tc.counters, 0, cnt);
+      if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemset");
+    }
+    if (!rc) {
+      h->tc.ready = sgemv::tc_encode_weights(h->L, h->d_vals, h->d_idx, h->d_sz, &h->tc);
+      if (!h->tc.ready)
+        rc = fail(SGEMV_ERR_CUDA, "encoding the tensor maps of the packed weight failed");
+    }
   }
   if (rc) {
     free_ctx(h);
@@ -423,7 +442,12 @@ static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s)
   }
   // m = 1: the CUDA-core table kernel; m >= 2: the sparse tensor-core kernel
   // (1:4 as 2:4 with a zero partner per quad)
+#ifdef SGEMV_BATCH_MMA_SYNC
+  // build option: the warp-level mma.sp batch kernel instead of tcgen05
   cudaError_t e = m == 1 ? sgemv::launch_m1(L, a, s) : sgemv::launch_mma(L, a, s);
+#else
+  cudaError_t e = m == 1 ? sgemv::launch_m1(L, a, s) : sgemv::launch_tc(L, a, h->tc, s);
+#endif
   if (e == cudaErrorNotSupported) {
     (void)cudaGetLastError();
     return fail(SGEMV_ERR_UNSUPPORTED,

@@ -20,11 +20,12 @@
 //            a multiple of 4 groups (16-byte aligned rows).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/sgemv.h"
+#include "sgemv.h"
 
 namespace sgemv {
 
@@ -40,6 +41,15 @@ struct Layout {
   int64_t gstride;     // scale/zero words per row in memory: multiple of 4
   int64_t vals_row;    // canonical bytes per row
   int64_t idx_row;
+};
+
+// Tensor maps of a packed weight for the tensor-core batch kernel, and its
+// split-K workspace (fp32 partial tiles) and per-tile arrival counters.
+struct TcMaps {
+  CUtensorMap vals, idx, sz;
+  float* scratch;
+  int* counters;
+  bool ready;
 };
 
 }  // namespace sgemv
@@ -64,6 +74,7 @@ struct sgemv_ctx {
   int64_t* d_goff;     // rows + 1 canonical scale/zero offsets
   int64_t canon_groups;  // canonical scale/zero entries of the whole matrix
   int withhold_runs;     // failure-detection test hook: runs left to sabotage
+  sgemv::TcMaps tc;      // batch kernel (2 <= m): weight maps and split-K workspace
 };
 
 namespace sgemv {
@@ -113,6 +124,12 @@ cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s);
 // m = 1 over several matrices sharing x, cols and N in one launch.
 cudaError_t launch_m1_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s);
 int max_group();
+// Tensor-core batch kernel (sgemv_tc.cu), 2 <= m <= 64.
+size_t tc_scratch_bytes(int max_m);
+int tc_tiles(const Layout& L);
+bool tc_encode_weights(const Layout& L, const uint4* vals, const uint2* idx, const uint32_t* sz,
+                       TcMaps* maps);
+cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s);
 // Whether a product of m rows on this layout runs a kernel with the bounded
 // split-K wait that the failure-detection hook can make run out.
 bool withhold_applies(const Layout& L, int m);

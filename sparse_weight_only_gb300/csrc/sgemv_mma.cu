@@ -643,7 +643,12 @@ int g_sms[64] = {0};
 }  // namespace
 
 bool withhold_applies(const Layout& L, int m) {
+#ifdef SGEMV_BATCH_MMA_SYNC
   return m >= 2 && push_reduce((m + 7) / 8) && L.rows > 0 && L.cols > 0;
+#else
+  // the tensor-core kernel's x loads (every batch size)
+  return m >= 2 && L.rows > 0 && L.cols > 0;
+#endif
 }
 
 cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s) {

@@ -1,0 +1,767 @@
+// sgemv_tc.cu -- SparseGemv for a batch of activation rows (2 <= m <= 64:
+// beam candidates / prefix-tree verification nodes) on the fifth-generation
+// tensor cores: tcgen05.mma.sp with the accumulators in tensor memory.
+//
+// Product (Dong et al., arXiv 2605.11582, section 1 contribution 2 and
+// section 3.3, applied to the verification batch of section 3.1):
+//   y[m][r] = sum_G s_rG * sum_{kept j in G} (q_j - z_rG) * x[m][col_j],
+// each product exact, fp32 accumulation, one binary16 rounding per output.
+//
+// The weight is the MMA's A operand (M = 128 weight rows per tile), x the B
+// operand (N = m rounded up to 16), and the 2:4 sparse MMA consumes the
+// stored in-quad positions directly as its metadata:
+//  * A: each thread owns one weight row (= one tensor-memory lane) and
+//    decodes its kept weights to exact binary16 (q - z) -- PRMT + LOP3 +
+//    HSUB2 per quad, an integer in [-15, 15] -- then writes them to tensor
+//    memory with tcgen05.st; one tensor-memory column holds one quad's two
+//    kept values.  1:4 weights pair each kept value with a zero at the other
+//    position of its half of the quad, so the 2:4 MMA computes exactly its
+//    product.
+//  * metadata: the 2:4 position nibbles a | b << 2 of a row's eight quads of
+//    a 32-column k-step are one 32-bit word; tensor memory holds them as the
+//    warp-level sparse MMA does in registers -- within each 16 rows, lane i
+//    (i < 8) carries quads 0..3 of rows i and i + 8, lane i + 8 quads 4..7
+//    -- so each row thread exchanges half of its word with lane ^ 8.
+//  * B: x arrives by TMA in 128-byte-swizzled K-major tiles, 64 columns per
+//    tile, one shared-memory descriptor per 32-column k-step.
+//  * scale: every quantisation group's k-steps accumulate into a tensor-memory
+//    block of their own; the row threads load it (tcgen05.ld), multiply by
+//    the group's fp32 scale and add into fp32 registers.
+//  * weights: a unit of 4 chunks (256 columns at 2:4, 512 at 1:4) of 128 rows
+//    comes in by three TMA tile loads (positions, codes, scale/zero words)
+//    into a ring of shared-memory stages filled well ahead of use.
+//  * work split: a persistent grid of one CTA per SM takes equal runs of the
+//    (row tile, K unit) sequence.  A tile whose units span several CTAs is
+//    finished by the last of them to arrive: each writes its fp32 partial to
+//    the handle's split-K workspace and bumps the tile's counter; the last
+//    sums the partials in CTA order (deterministic) and writes y.  No CTA
+//    ever waits for another.
+//  * every wait on an mbarrier is bounded; one that runs out records
+//    SGEMV_ERR_TIMEOUT, the CTA stops issuing work, lets the copies it
+//    issued land and frees its tensor memory.
+#include <cuda.h>
+#include <string.h>
+
+#include "sgemv_internal.cuh"
+
+namespace sgemv {
+namespace {
+
+constexpr int kThreads = 256;          // 8 warps: lane quadrant w % 4, k-step half w / 4
+constexpr int kRows = 128;             // weight rows per tile (MMA M)
+constexpr int kNW = 6;                 // weight units in the shared-memory ring
+constexpr int kNX = 4;                 // x sub-stages in the ring
+constexpr int kTmemCols = 512;
+constexpr int kDCols = 256;            // accumulator blocks live in columns [0, 256)
+// one weight unit: codes 128 rows x 64 B (64-byte swizzle) | positions
+// 128 x 32 B (32-byte swizzle) | scale/zero words 128 x 32 B
+constexpr int kStageW = 16384;
+constexpr int kValsOff = 0, kIdxOff = 8192, kSzOff = 12288;
+constexpr int kSzWords = 8;            // scale/zero words per row and unit
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr unsigned long long kInjectWaitNs = 20000ull;
+
+struct TcParams {
+  CUtensorMap tm_vals, tm_idx, tm_sz, tm_x;
+  __half* y;
+  float* scratch;        // [grid][2][128][npad] fp32 partial tiles
+  int* counters;         // [ntiles] arrivals per tile (left at 0)
+  int* err;
+  int rows, cols, m;
+  int group, gshift;
+  int ntiles, units_per_tile;
+  long long total_units;
+  int grid;
+  int withhold;          // failure-detection test hook: no x loads are issued
+  unsigned long long wait_ns;
+};
+
+// ---- PTX helpers -----------------------------------------------------------
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 128-byte-swizzled K-major shared-memory operand (8-row atoms, 1024 B apart)
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFF) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ void mma_sp(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t meta,
+                                       uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %5, 0;\n"
+      " tcgen05.mma.sp.cta_group::1.kind::f16 [%0], [%1], %2, [%3], %4, p;\n}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(meta), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+               "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void ld8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                 "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// ---- decode ---------------------------------------------------------------
+// (1024 + z, 64 + z) as half2 from a scale/zero word (zero in the high half)
+__device__ __forceinline__ uint32_t zconst(uint32_t szw) {
+  const uint32_t zz = __byte_perm(szw, 0u, 0x3232u);
+  uint32_t zc;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(zc) : "r"(zz), "r"(0x54006400u));
+  return zc;
+}
+// 2:4: half2 (q_a - z, q_b - z) of the quad in byte `b` of w: the byte goes to
+// bytes 0 and 2, its low nibble into the mantissa of 1024, its high nibble
+// into that of 64, and one subtraction removes (1024 + z, 64 + z).
+__device__ __forceinline__ uint32_t quad24(uint32_t w, int b, uint32_t zc) {
+  uint32_t t = __byte_perm(w, 0u, 0x4040u | (uint32_t)b | ((uint32_t)b << 8));
+  asm("lop3.b32 %0, %1, 0x00F0000F, 0x54006400, 0xEA;" : "=r"(t) : "r"(t));
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(zc));
+  return d;
+}
+// 1:4: the A words of quads c and c + 4 (c < 4) of a k-step: the nibbles of
+// word w (one per quad) decode pairwise, and each value goes to the low half
+// (even position) or high half (odd position) of its word, the other half 0.
+__device__ __forceinline__ void quads14(uint32_t w, int c, uint32_t pos, uint32_t z1024,
+                                        uint32_t& a_c, uint32_t& a_c4) {
+  uint32_t t;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(t) : "r"(w >> (4 * c)));
+  uint32_t v;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(t), "r"(z1024));   // (v_c, v_c4)
+  const uint32_t odd_c = (pos >> (2 * c)) & 1u, odd_c4 = (pos >> (2 * c + 8)) & 1u;
+  a_c = __byte_perm(v, 0u, 0x4410u - odd_c * 0x33CCu);    // (v,0) or (0,v)
+  a_c4 = __byte_perm(v, 0u, 0x4432u - odd_c4 * 0x11EEu);
+}
+// 1:4 metadata word of a k-step from its 16 position bits (quad c at bits
+// 2c): nibble c is 4 = (0, 1) when the position is 0 or 1, else 14 = (2, 3).
+__device__ __forceinline__ uint32_t meta14(uint32_t pos16) {
+  uint32_t x = (pos16 >> 1) & 0x5555u;            // high bit of quad c at bit 2c
+  x = (x | (x << 8)) & 0x00FF00FFu;
+  x = (x | (x << 4)) & 0x0F0F0F0Fu;
+  x = (x | (x << 2)) & 0x33333333u;
+  x = (x | (x << 1)) & 0x55555555u;               // ... at bit 4c
+  return 0x44444444u | (x * 10u);
+}
+// The tensor-memory lane word of a row's metadata word (lane ^ 8 exchange).
+__device__ __forceinline__ uint32_t meta_lane(uint32_t mw, int lane) {
+  const uint32_t p = __shfl_xor_sync(0xffffffffu, mw, 8);
+  return (lane & 8) ? __byte_perm(p, mw, 0x7632u) : __byte_perm(mw, p, 0x5410u);
+}
+
+// ---- the kernel -----------------------------------------------------------
+// Sequence of the CTA's work: units u in [u_begin, u_end) of the linear
+// (tile, unit) order; each unit is SUBS sub-stages of four 32-column
+// k-steps.  A "segment" is the CTA's run of units inside one tile; a group
+// "instance" is a maximal run of the segment's k-steps inside one
+// quantisation group and owns one accumulator block.
+template <int N, int NPAD>
+__global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcParams p) {
+  constexpr int SUBS = N == 2 ? 2 : 4;           // sub-stages per unit
+  constexpr int UNIT_COLS = 128 * SUBS;          // 256 or 512 dense columns
+  constexpr int XBOX = NPAD * 128;               // bytes of one 64-column x tile
+  constexpr int XSUB = 2 * XBOX;
+  constexpr int ND = kDCols / NPAD;              // accumulator blocks
+  constexpr int HALF = NPAD / 2;                 // accumulator columns per thread
+  constexpr uint32_t IDESC = (1u << 2) | (1u << 4) | ((uint32_t)(NPAD >> 3) << 17) |
+                             ((uint32_t)(kRows >> 4) << 24);
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* sm = smem_raw + (base - raw);
+  const uint32_t wring = base;
+  const uint32_t xring = base + kNW * kStageW;
+  const uint32_t bars = xring + kNX * XSUB;
+  const uint32_t bar_w = bars;                    // kNW  weight unit landed
+  const uint32_t bar_x = bars + 8 * kNW;          // kNX  x sub-stage landed
+  const uint32_t bar_a = bar_x + 8 * kNX;         // 2    MMAs of an A/metadata slot done
+  const uint32_t bar_d = bar_a + 16;              // ND   accumulator block ready
+  const uint32_t misc = bar_d + 8 * ND;           // tmem base, abort flag, last-arriver flag
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + (misc - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + (misc - base) + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(sm + (misc - base) + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, h = warp >> 2;
+  const int r = quad * 32 + lane;                 // this thread's row of the tile
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+
+  const int U = p.units_per_tile;
+  const long long T = p.total_units;
+  const int P = p.grid;
+  const long long u_begin = (long long)blockIdx.x * T / P;
+  const long long u_end = (long long)(blockIdx.x + 1) * T / P;
+  const int nunits = (int)(u_end - u_begin);
+  const int nsub = nunits * SUBS;
+
+  if (tid == 0) {
+    for (int i = 0; i < kNW; ++i) mbar_init(bar_w + 8 * i, 1);
+    for (int i = 0; i < kNX; ++i) mbar_init(bar_x + 8 * i, 1);
+    mbar_init(bar_a, 1);
+    mbar_init(bar_a + 8, 1);
+    for (int i = 0; i < ND; ++i) mbar_init(bar_d + 8 * i, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(misc),
+                 "n"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- producer state (thread 0) ----
+  int w_issued = 0, x_issued = 0;
+  auto issue_w = [&](int ui) {   // weight unit ui (CTA-local) into slot ui % kNW
+    const long long ug = u_begin + ui;
+    const int tile = (int)(ug / U), uit = (int)(ug % U);
+    const uint32_t dst = wring + (uint32_t)((ui % kNW) * kStageW);
+    const uint32_t bar = bar_w + 8 * (ui % kNW);
+    mbar_expect_tx(bar, kStageW);
+    const int chunk0 = uit * 4;
+    const int g0 = ((uit * UNIT_COLS) >> p.gshift) & ~3;
+    tma_2d(dst + kValsOff, &p.tm_vals, chunk0 * 16, tile * kRows, bar);
+    tma_2d(dst + kIdxOff, &p.tm_idx, chunk0 * 8, tile * kRows, bar);
+    tma_2d(dst + kSzOff, &p.tm_sz, g0, tile * kRows, bar);
+  };
+  auto issue_x = [&](int s) {    // x of sub-stage s into slot s % kNX
+    const long long ug = u_begin + s / SUBS;
+    const int uit = (int)(ug % U);
+    const int col0 = uit * UNIT_COLS + (s % SUBS) * 128;
+    const uint32_t dst = xring + (uint32_t)((s % kNX) * XSUB);
+    const uint32_t bar = bar_x + 8 * (s % kNX);
+    mbar_expect_tx(bar, XSUB);
+    tma_2d(dst, &p.tm_x, col0, 0, bar);
+    tma_2d(dst + XBOX, &p.tm_x, col0 + 64, 0, bar);
+  };
+  // bounded wait: false when it ran out (abort set) or another thread aborted
+  auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try(bar, parity)) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > p.wait_ns) {
+        *abort_flag = 1;
+        atomicCAS(p.err, 0, kDevErrTimeout);
+        return false;
+      }
+    }
+    return true;
+  };
+
+  if (tid == 0) {
+    for (int ui = 0; ui < min(nunits, kNW - 1); ++ui) issue_w(ui);
+    w_issued = min(nunits, kNW - 1);
+  }
+  // x and the split-K workspace may be in use by the previous kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (tid == 0 && !p.withhold) {
+    for (int s = 0; s < min(nsub, kNX - 1); ++s) issue_x(s);
+    x_issued = min(nsub, kNX - 1);
+  }
+
+  float acc[HALF];
+#pragma unroll
+  for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
+  // instances that ended in the previous sub-stage: block and this row's scale
+  int pend_n = 0;
+  int pend_blk[2] = {0, 0};
+  uint32_t pend_par[2] = {0, 0};
+  float pend_s[2] = {0.0f, 0.0f};
+  int inst = -1;                   // instance index of the CTA (block = inst % ND)
+  bool first_seg = true;
+  int seg_tile = -1, seg_u0 = 0;   // current segment: tile, first unit in the tile
+
+  // epilogue of one finished instance: acc += s * D[block]
+  auto drain = [&](int blk, uint32_t par, float s) {
+    wait(bar_d + 8 * blk, par);
+    fence_after();
+    const uint32_t taddr = tmem + lane_off + (uint32_t)(blk * NPAD + h * HALF);
+    uint32_t v[HALF];
+#pragma unroll
+    for (int c8 = 0; c8 < HALF / 8; ++c8) {
+      uint32_t (&v8)[8] = *reinterpret_cast<uint32_t (*)[8]>(v + 8 * c8);
+      ld8(taddr + 8 * c8, v8);
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < HALF; ++i) acc[i] = fmaf(s, __uint_as_float(v[i]), acc[i]);
+  };
+  // split-K arrivals of this CTA's partial segments (the first and the last)
+  bool counted[2] = {false, false};
+  int s_mma = 0;   // sub-stages whose MMAs thread 0 issued
+
+  for (int s = 0; s < nsub; ++s) {
+    const int ui = s / SUBS, ls = s % SUBS;
+    const long long ug = u_begin + ui;
+    const int tile = (int)(ug / U), uit = (int)(ug % U);
+    if (tile != seg_tile) {
+      seg_tile = tile;
+      seg_u0 = uit;
+    }
+    const int seg_u1 = (int)min((long long)U, u_end - (long long)tile * U);   // units end
+    const int seg_c0 = seg_u0 * UNIT_COLS;
+    const int seg_c1 = min(p.cols, seg_u1 * UNIT_COLS);
+    const int scol0 = uit * UNIT_COLS + ls * 128;
+    const uint32_t wslot = wring + (uint32_t)((ui % kNW) * kStageW);
+    const int t = s & 1;
+
+    if (ls == 0) wait(bar_w + 8 * (ui % kNW), (uint32_t)((ui / kNW) & 1));
+
+    // ---- decode this thread's two k-steps (2h, 2h + 1) of the sub-stage
+    const int g0 = ((uit * UNIT_COLS) >> p.gshift) & ~3;
+    const int myG = (scol0 + 64 * h) >> p.gshift;
+    const uint32_t szw = lds32(wslot + kSzOff + (uint32_t)(r * 32 + (myG - g0) * 4));
+    uint32_t a0[8], a1[8];
+    uint32_t m0, m1;
+    if constexpr (N == 2) {
+      const int ch = 2 * ls + h;                              // chunk of the unit
+      const uint4 v = lds128(wslot + kValsOff + (uint32_t)(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
+      const uint2 ix = lds64(wslot + kIdxOff +
+                             (uint32_t)(r * 32 + ((ls ^ ((r >> 2) & 1)) << 4) + h * 8));
+      const uint32_t zc = zconst(szw);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        a0[c] = quad24(c < 4 ? v.x : v.y, c & 3, zc);
+        a1[c] = quad24(c < 4 ? v.z : v.w, c & 3, zc);
+      }
+      m0 = ix.x;
+      m1 = ix.y;
+    } else {
+      const uint2 v = lds64(wslot + kValsOff +
+                            (uint32_t)(r * 64 + ((ls ^ ((r >> 1) & 3)) << 4) + h * 8));
+      const uint32_t pw = lds32(wslot + kIdxOff +
+                                (uint32_t)(r * 32 + (((ls >> 1) ^ ((r >> 2) & 1)) << 4) +
+                                           (ls & 1) * 8 + h * 4));
+      const uint32_t z1024 = __byte_perm(zconst(szw), 0u, 0x1010u);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        quads14(v.x, c, pw, z1024, a0[c], a0[c + 4]);
+        quads14(v.y, c, pw >> 16, z1024, a1[c], a1[c + 4]);
+      }
+      m0 = meta14(pw & 0xFFFFu);
+      m1 = meta14(pw >> 16);
+    }
+    m0 = meta_lane(m0, lane);
+    m1 = meta_lane(m1, lane);
+
+    // ---- into the A / metadata slot t (free once the MMAs of s - 2 are done)
+    if (s >= 2) wait(bar_a + 8 * t, (uint32_t)(((s - 2) >> 1) & 1));
+    fence_after();
+    const uint32_t slot_col = (uint32_t)(kDCols + 32 * (4 * t + 2 * h));
+    st8(tmem + lane_off + slot_col + 8, a0);
+    st8(tmem + lane_off + slot_col + 32 + 8, a1);
+    st1(tmem + lane_off + slot_col, m0);
+    st1(tmem + lane_off + slot_col + 32, m1);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    fence_before();
+    __syncthreads();
+    const bool aborted = *abort_flag != 0;
+    if (aborted) break;
+
+    // ---- instances of this sub-stage (the same walk in every thread)
+    int ij[4];
+    uint32_t first[4];
+    bool valid[4], ends[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = scol0 + 32 * j;
+      valid[j] = col < seg_c1;
+      first[j] = 0;
+      ends[j] = false;
+      if (valid[j]) {
+        if (col == seg_c0 || (col & (p.group - 1)) == 0) {
+          ++inst;
+          first[j] = 1;
+        }
+        ends[j] = col + 32 >= seg_c1 || ((col + 32) & (p.group - 1)) == 0;
+      }
+      ij[j] = inst;
+    }
+
+    // ---- thread 0: the MMAs of this sub-stage and the loads ahead
+    if (tid == 0) {
+      fence_after();
+      if (wait(bar_x + 8 * (s % kNX), (uint32_t)((s / kNX) & 1))) {
+        const uint32_t xb = xring + (uint32_t)((s % kNX) * XSUB);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (!valid[j]) continue;
+          const uint32_t col = (uint32_t)(kDCols + 32 * (4 * t + j));
+          mma_sp(tmem + (uint32_t)((ij[j] % ND) * NPAD), tmem + col + 8,
+                 desc_sw128(xb + (uint32_t)((j >> 1) * XBOX + (j & 1) * 64)), tmem + col, IDESC,
+                 first[j] ? 0u : 1u);
+        }
+        mma_commit(bar_a + 8 * t);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (valid[j] && ends[j]) mma_commit(bar_d + 8 * (ij[j] % ND));
+        ++s_mma;
+      }
+      // x for sub-stage s + kNX - 1 reuses the slot of s - 1
+      if (!p.withhold && x_issued < nsub && !*abort_flag) {
+        if (s >= 1) wait(bar_a + 8 * ((s - 1) & 1), (uint32_t)(((s - 1) >> 1) & 1));
+        if (!*abort_flag) issue_x(x_issued++);
+      }
+      // weights for unit ui + kNW - 1 reuse the slot of ui - 1 (read before the barrier above)
+      if (ls == 0 && w_issued < nunits && !*abort_flag) issue_w(w_issued++);
+    }
+
+    // ---- epilogue of the instances that ended in the previous sub-stage
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (i < pend_n) drain(pend_blk[i], pend_par[i], pend_s[i]);
+    pend_n = 0;
+    // instances ending here: block, phase and this row's scale (at most two)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (valid[j] && ends[j]) {
+        const int G = (scol0 + 32 * j) >> p.gshift;
+        const uint32_t w = lds32(wslot + kSzOff + (uint32_t)(r * 32 + (G - g0) * 4));
+        const float sc = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+        if (pend_n == 0) {
+          pend_blk[0] = ij[j] % ND;
+          pend_par[0] = (uint32_t)((ij[j] / ND) & 1);
+          pend_s[0] = sc;
+        } else {
+          pend_blk[1] = ij[j] % ND;
+          pend_par[1] = (uint32_t)((ij[j] / ND) & 1);
+          pend_s[1] = sc;
+        }
+        ++pend_n;
+      }
+    }
+
+    // ---- end of a segment: finish it and write y (directly, or through the
+    // split-K workspace when the tile is shared with other CTAs)
+    const bool seg_end = ls == SUBS - 1 && (ug + 1 == u_end || (ug + 1) / U != tile);
+    if (seg_end) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (i < pend_n) drain(pend_blk[i], pend_par[i], pend_s[i]);
+      pend_n = 0;
+      const int row = tile * kRows + r;
+      const bool full = seg_u0 == 0 && seg_u1 == U;
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < HALF; ++i) {
+          const int mm = h * HALF + i;
+          if (mm < p.m && row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(acc[i]);
+        }
+      } else {
+        const int slot = first_seg ? 0 : 1;
+        float* dst = p.scratch + (((size_t)blockIdx.x * 2 + slot) * kRows + r) * NPAD + h * HALF;
+#pragma unroll
+        for (int i = 0; i < HALF; i += 4)
+          __stcg(reinterpret_cast<float4*>(dst + i), make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]));
+        __threadfence();
+        __syncthreads();
+        counted[slot] = true;
+        if (tid == 0) {
+          const long long tu0 = (long long)tile * U, tu1 = tu0 + U - 1;
+          const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu1 + 1) * P - 1) / T);
+          const int old = atomicAdd(p.counters + tile, 1);
+          *last_flag = old == c1 - c0;
+          if (old == c1 - c0) p.counters[tile] = 0;   // left at 0 for the next launch
+        }
+        __syncthreads();
+        if (*last_flag) {
+          __threadfence();
+          const long long tu0 = (long long)tile * U, tu1 = tu0 + U - 1;
+          const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu1 + 1) * P - 1) / T);
+          float sum[HALF];
+#pragma unroll
+          for (int i = 0; i < HALF; ++i) sum[i] = 0.0f;
+          for (int c = c0; c <= c1; ++c) {
+            const long long bc = (long long)c * T / P;
+            const int cslot = bc >= tu0 ? 0 : 1;     // the tile is CTA c's first, or its last
+            const float* src = p.scratch + (((size_t)c * 2 + cslot) * kRows + r) * NPAD + h * HALF;
+#pragma unroll
+            for (int i = 0; i < HALF; i += 4) {
+              const float4 f = __ldcg(reinterpret_cast<const float4*>(src + i));
+              sum[i] += f.x;
+              sum[i + 1] += f.y;
+              sum[i + 2] += f.z;
+              sum[i + 3] += f.w;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < HALF; ++i) {
+            const int mm = h * HALF + i;
+            if (mm < p.m && row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(sum[i]);
+          }
+        }
+      }
+      first_seg = false;
+#pragma unroll
+      for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
+    }
+  }
+
+  // ---- teardown.  After an abort: the copies and MMAs this CTA issued are
+  // let land (bounded) before its shared and tensor memory are released --
+  // only the last load issued into each slot and the last two MMA batches can
+  // still be in flight -- and the split-K counters of its partial tiles that
+  // it never reached are brought back to zero, so the next launch counts
+  // right (y of this launch is undefined).
+  fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {
+    const unsigned long long lim = p.wait_ns;
+    auto settle = [&](uint32_t bar, uint32_t par) {
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try(bar, par))
+        if (global_ns() - t0 > lim) break;
+    };
+    for (int ui = max(0, w_issued - kNW); ui < w_issued; ++ui)
+      settle(bar_w + 8 * (ui % kNW), (uint32_t)((ui / kNW) & 1));
+    for (int x = max(0, x_issued - kNX); x < x_issued; ++x)
+      settle(bar_x + 8 * (x % kNX), (uint32_t)((x / kNX) & 1));
+    for (int x = max(0, s_mma - 2); x < s_mma; ++x)
+      settle(bar_a + 8 * (x & 1), (uint32_t)((x >> 1) & 1));
+    const int t_first = (int)(u_begin / U), t_last = (int)((u_end - 1) / U);
+    for (int k = 0; k < 2; ++k) {
+      const int tile = k == 0 ? t_first : t_last;
+      if (k == 1 && t_last == t_first) break;
+      const long long tu0 = (long long)tile * U;
+      const bool partial = k == 0 ? (u_begin > tu0 || u_end < tu0 + U) : (u_end < tu0 + U);
+      if (!partial || counted[k]) continue;
+      const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu0 + U) * P - 1) / T);
+      if (atomicAdd(p.counters + tile, 1) == c1 - c0) p.counters[tile] = 0;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+}  // namespace sgemv
+
+// ---- host side --------------------------------------------------------------
+namespace sgemv {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// A 2-D map over a row-major array of `rows` rows of `inner` elements.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* ptr,
+               uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+               CUtensorMapSwizzle sw, CUtensorMapL2promotion l2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !ptr || inner == 0 || rows == 0) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * (uint64_t)esize};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_tc_sms[64] = {0};
+
+int tc_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!g_tc_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_tc_sms[dev] = n;
+  }
+  return g_tc_sms[dev];
+}
+
+int npad_of(int m) { return ((m + 15) / 16) * 16; }
+
+size_t tc_smem(int npad) {
+  // 1024 alignment slack + weight ring + x ring + barriers and flags; at
+  // least 120 KB, so that one CTA (and one tensor-memory allocation) per SM
+  const size_t need = 1024 + (size_t)kNW * kStageW + (size_t)kNX * 2 * npad * 128 + 512;
+  return need < 120 * 1024 ? 120 * 1024 : need;
+}
+
+template <int N, int NPAD>
+cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s) {
+  constexpr int UNIT_COLS = N == 2 ? 256 : 512;
+  const int sms = tc_sms();
+  if (sms <= 0) return cudaErrorNotSupported;
+  TcParams p;
+  memset(&p, 0, sizeof p);
+  p.tm_vals = maps.vals;
+  p.tm_idx = maps.idx;
+  p.tm_sz = maps.sz;
+  if (!encode_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x, (uint64_t)L.cols,
+                 (uint64_t)a.m, 64, NPAD, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return cudaErrorInvalidValue;
+  p.y = a.y;
+  p.scratch = maps.scratch;
+  p.counters = maps.counters;
+  p.err = a.err;
+  p.rows = L.rows;
+  p.cols = L.cols;
+  p.m = a.m;
+  p.group = L.group;
+  p.gshift = L.group == 64 ? 6 : (L.group == 128 ? 7 : 8);
+  p.ntiles = (L.rows + kRows - 1) / kRows;
+  p.units_per_tile = (L.cols + UNIT_COLS - 1) / UNIT_COLS;
+  p.total_units = (long long)p.ntiles * p.units_per_tile;
+  p.grid = (int)(p.total_units < sms ? p.total_units : sms);
+  p.withhold = a.withhold;
+  p.wait_ns = a.withhold ? kInjectWaitNs : kWaitLimitNs;
+  const size_t smem = tc_smem(NPAD);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_tc<N, NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_tc<N, NPAD>, p);
+}
+
+}  // namespace
+
+size_t tc_scratch_bytes(int max_m) {
+  if (max_m < 2) return 0;
+  const int sms = tc_sms();
+  return (size_t)(sms > 0 ? sms : 0) * 2 * kRows * npad_of(max_m) * sizeof(float);
+}
+
+int tc_tiles(const Layout& L) { return (L.rows + kRows - 1) / kRows; }
+
+bool tc_encode_weights(const Layout& L, const uint4* vals, const uint2* idx, const uint32_t* sz,
+                       TcMaps* maps) {
+  if (L.rows == 0 || L.cols == 0) return false;
+  return encode_2d(&maps->vals, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vals, (uint64_t)L.cstride * 16,
+                   (uint64_t)L.rows, 64, kRows, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
+         encode_2d(&maps->idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, idx, (uint64_t)L.cstride * 8,
+                   (uint64_t)L.rows, 32, kRows, CU_TENSOR_MAP_SWIZZLE_32B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
+         encode_2d(&maps->sz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, sz, (uint64_t)L.gstride,
+                   (uint64_t)L.rows, kSzWords, kRows, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+}
+
+cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s) {
+  if (a.m < 2 || a.m > 64 || L.rows == 0 || L.cols == 0 || !maps.ready || !maps.scratch ||
+      !maps.counters)
+    return cudaErrorNotSupported;
+  if (((uintptr_t)a.x & 15u) != 0) return cudaErrorNotSupported;
+  const int np = npad_of(a.m);
+  if (L.n_keep == 2) {
+    switch (np) {
+      case 16: return launch_tc_n<2, 16>(L, a, maps, s);
+      case 32: return launch_tc_n<2, 32>(L, a, maps, s);
+      case 48: return launch_tc_n<2, 48>(L, a, maps, s);
+      default: return launch_tc_n<2, 64>(L, a, maps, s);
+    }
+  }
+  switch (np) {
+    case 16: return launch_tc_n<1, 16>(L, a, maps, s);
+    case 32: return launch_tc_n<1, 32>(L, a, maps, s);
+    case 48: return launch_tc_n<1, 48>(L, a, maps, s);
+    default: return launch_tc_n<1, 64>(L, a, maps, s);
+  }
+}
+
+}  // namespace sgemv

@@ -1,11 +1,12 @@
 """Failure detection on the GPU without a GPU fault.
 
-The small-batch kernel's split-K reduction is the library's one device-side
-wait on other CTAs, and it is bounded.  The test hook sgemv_debug_withhold
-makes every cluster rank withhold its partial sums (nothing is sent, so no
-remote store is in flight) and shortens the limit: the wait runs out, the
-kernel records SGEMV_ERR_TIMEOUT in the handle's error word and returns, and
-the device stays usable -- the next call is correct.
+Every wait of the batch kernel (2 <= m <= 64) on its own copies and MMAs is
+bounded.  The test hook sgemv_debug_withhold makes the kernel withhold its x
+loads (nothing is in flight that it would have to wait for) and shortens the
+limit: the wait runs out, the kernel records SGEMV_ERR_TIMEOUT in the
+handle's error word, lets the copies it did issue land, frees its tensor
+memory and returns, and the device stays usable -- the next calls are
+correct, including tiles whose split-K counters the aborted launch left.
 """
 import numpy as np
 import pytest
@@ -33,10 +34,10 @@ def _run(h, x):
     return y
 
 
-@pytest.mark.parametrize("m", [2, 4, 16])
+@pytest.mark.parametrize("m", [2, 4, 16, 33, 64])
 def test_bounded_wait_runs_out_and_recovers(native, orc, m):
     rows, cols = 256, 4096          # two row tiles: clusters of several ranks
-    h, p = _setup(native, orc, rows, cols, 2, 128, max_m=16)
+    h, p = _setup(native, orc, rows, cols, 2, 128, max_m=64)
     x = synth.activations(40 + m, m, cols)
     norms = np.abs(orc.dequant(p)).sum(axis=1)
 
@@ -44,7 +45,7 @@ def test_bounded_wait_runs_out_and_recovers(native, orc, m):
     _run(h, x)
     torch.cuda.synchronize()
     assert h.status() == native.SGEMV_ERR_TIMEOUT
-    assert "split-K" in native.load().sgemv_last_error().decode()
+    assert "gave up" in native.load().sgemv_last_error().decode()
     assert h.status() == native.SGEMV_OK      # the word was cleared
 
     for _ in range(2):                         # later calls run normally
@@ -54,24 +55,41 @@ def test_bounded_wait_runs_out_and_recovers(native, orc, m):
         check_y(orc, y.cpu().numpy(), orc.matvec(p, x), norms, f"after timeout m={m}")
 
 
-def test_withhold_leaves_other_kernels_alone(native, orc):
-    """m = 1 and the pulled reduction (m > 16) have no such wait: the hook
-    is not consumed by them and their results stay exact."""
+def test_withhold_leaves_m1_alone(native, orc):
+    """m = 1 has no such wait: the hook is not consumed by it and its result
+    stays exact; the pending hook fires on the next batch call."""
     rows, cols = 256, 4096
     h, p = _setup(native, orc, rows, cols, 2, 128, max_m=64)
     norms = np.abs(orc.dequant(p)).sum(axis=1)
     h.debug_withhold(1)
-    for m in (1, 33):
-        x = synth.activations(70 + m, m, cols)
-        y = _run(h, x)
-        torch.cuda.synchronize()
-        assert h.status() == native.SGEMV_OK
-        check_y(orc, y.cpu().numpy(), orc.matvec(p, x), norms, f"m={m}")
-    # the pending hook still fires on the next eligible call
+    x = synth.activations(71, 1, cols)
+    y = _run(h, x)
+    torch.cuda.synchronize()
+    assert h.status() == native.SGEMV_OK
+    check_y(orc, y.cpu().numpy(), orc.matvec(p, x), norms, "m=1")
     _run(h, synth.activations(5, 4, cols))
     torch.cuda.synchronize()
     assert h.status() == native.SGEMV_ERR_TIMEOUT
     h.debug_withhold(0)
+
+
+def test_timeout_in_a_1of4_multi_tile_matrix_recovers(native, orc):
+    """A larger 1:4 matrix, many CTAs sharing tiles: after the aborted launch
+    every tile's split-K counter is back at zero, so the next results are
+    exact."""
+    rows, cols = 1100, 4096
+    h, p = _setup(native, orc, rows, cols, 1, 64, max_m=8)
+    norms = np.abs(orc.dequant(p)).sum(axis=1)
+    x = synth.activations(90, 8, cols)
+    h.debug_withhold(1)
+    _run(h, x)
+    torch.cuda.synchronize()
+    assert h.status() == native.SGEMV_ERR_TIMEOUT
+    for _ in range(2):
+        y = _run(h, x)
+        torch.cuda.synchronize()
+        assert h.status() == native.SGEMV_OK
+        check_y(orc, y.cpu().numpy(), orc.matvec(p, x), norms, "1:4 after timeout")
 
 
 def test_withhold_rejects_negative(native):
