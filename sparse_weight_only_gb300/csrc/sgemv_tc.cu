@@ -50,7 +50,7 @@ namespace {
 constexpr int kThreads = 256;          // 8 warps: lane quadrant w % 4, k-step half w / 4
 constexpr int kRows = 128;             // weight rows per tile (MMA M)
 constexpr int kNW = 6;                 // weight units in the shared-memory ring
-constexpr int kNX = 4;                 // x sub-stages in the ring
+constexpr int kNX = 6;                 // x sub-stages in the ring (refilled 2 behind)
 constexpr int kTmemCols = 512;
 constexpr int kDCols = 256;            // accumulator blocks live in columns [0, 256)
 // one weight unit: codes 128 rows x 64 B (64-byte swizzle) | positions
@@ -274,29 +274,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // ---- producer state (thread 0) ----
+  // (tile, unit in tile) of the CTA's first unit: one 64-bit division here,
+  // then every walk over the units steps these forward in 32-bit arithmetic
+  const int tile0 = (int)(u_begin / U), uit0 = (int)(u_begin % U);
+
+  // ---- producer state (thread 0): the next weight unit and x sub-stage to
+  // load, each with its own (tile, unit) position
   int w_issued = 0, x_issued = 0;
-  auto issue_w = [&](int ui) {   // weight unit ui (CTA-local) into slot ui % kNW
-    const long long ug = u_begin + ui;
-    const int tile = (int)(ug / U), uit = (int)(ug % U);
-    const uint32_t dst = wring + (uint32_t)((ui % kNW) * kStageW);
-    const uint32_t bar = bar_w + 8 * (ui % kNW);
+  int w_tile = tile0, w_uit = uit0;
+  int x_uit = uit0, x_ls = 0;
+  auto issue_w = [&]() {   // weight unit w_issued into slot w_issued % kNW
+    const uint32_t dst = wring + (uint32_t)((w_issued % kNW) * kStageW);
+    const uint32_t bar = bar_w + 8 * (w_issued % kNW);
     mbar_expect_tx(bar, kStageW);
-    const int chunk0 = uit * 4;
-    const int g0 = ((uit * UNIT_COLS) >> p.gshift) & ~3;
-    tma_2d(dst + kValsOff, &p.tm_vals, chunk0 * 16, tile * kRows, bar);
-    tma_2d(dst + kIdxOff, &p.tm_idx, chunk0 * 8, tile * kRows, bar);
-    tma_2d(dst + kSzOff, &p.tm_sz, g0, tile * kRows, bar);
+    const int chunk0 = w_uit * 4;
+    const int g0 = ((w_uit * UNIT_COLS) >> p.gshift) & ~3;
+    tma_2d(dst + kValsOff, &p.tm_vals, chunk0 * 16, w_tile * kRows, bar);
+    tma_2d(dst + kIdxOff, &p.tm_idx, chunk0 * 8, w_tile * kRows, bar);
+    tma_2d(dst + kSzOff, &p.tm_sz, g0, w_tile * kRows, bar);
+    ++w_issued;
+    if (++w_uit == U) {
+      w_uit = 0;
+      ++w_tile;
+    }
   };
-  auto issue_x = [&](int s) {    // x of sub-stage s into slot s % kNX
-    const long long ug = u_begin + s / SUBS;
-    const int uit = (int)(ug % U);
-    const int col0 = uit * UNIT_COLS + (s % SUBS) * 128;
-    const uint32_t dst = xring + (uint32_t)((s % kNX) * XSUB);
-    const uint32_t bar = bar_x + 8 * (s % kNX);
+  auto issue_x = [&]() {   // x of sub-stage x_issued into slot x_issued % kNX
+    const int col0 = x_uit * UNIT_COLS + x_ls * 128;
+    const uint32_t dst = xring + (uint32_t)((x_issued % kNX) * XSUB);
+    const uint32_t bar = bar_x + 8 * (x_issued % kNX);
     mbar_expect_tx(bar, XSUB);
     tma_2d(dst, &p.tm_x, col0, 0, bar);
     tma_2d(dst + XBOX, &p.tm_x, col0 + 64, 0, bar);
+    ++x_issued;
+    if (++x_ls == SUBS) {
+      x_ls = 0;
+      if (++x_uit == U) x_uit = 0;
+    }
   };
   // bounded wait: false when it ran out (abort set) or another thread aborted
   auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -313,17 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     return true;
   };
 
-  if (tid == 0) {
-    for (int ui = 0; ui < min(nunits, kNW - 1); ++ui) issue_w(ui);
-    w_issued = min(nunits, kNW - 1);
-  }
+  if (tid == 0)
+    while (w_issued < min(nunits, kNW - 1)) issue_w();
   // x and the split-K workspace may be in use by the previous kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  if (tid == 0 && !p.withhold) {
-    for (int s = 0; s < min(nsub, kNX - 1); ++s) issue_x(s);
-    x_issued = min(nsub, kNX - 1);
-  }
+  if (tid == 0 && !p.withhold)
+    while (x_issued < min(nsub, kNX - 2)) issue_x();
 
   float acc[HALF];
 #pragma unroll
@@ -335,7 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   float pend_s[2] = {0.0f, 0.0f};
   int inst = -1;                   // instance index of the CTA (block = inst % ND)
   bool first_seg = true;
-  int seg_tile = -1, seg_u0 = 0;   // current segment: tile, first unit in the tile
+  int tile = tile0, uit = uit0;    // position of the current unit
+  int seg_u0 = uit0;               // first unit of the current segment in its tile
 
   // epilogue of one finished instance: acc += s * D[block]
   auto drain = [&](int blk, uint32_t par, float s) {
@@ -358,13 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
 
   for (int s = 0; s < nsub; ++s) {
     const int ui = s / SUBS, ls = s % SUBS;
-    const long long ug = u_begin + ui;
-    const int tile = (int)(ug / U), uit = (int)(ug % U);
-    if (tile != seg_tile) {
-      seg_tile = tile;
-      seg_u0 = uit;
+    if (ls == 0 && ui > 0 && ++uit == U) {   // next unit; a new tile starts a segment
+      uit = 0;
+      ++tile;
+      seg_u0 = 0;
     }
-    const int seg_u1 = (int)min((long long)U, u_end - (long long)tile * U);   // units end
+    const int seg_u1 = min(U, uit + (nunits - ui));   // the segment's units end
     const int seg_c0 = seg_u0 * UNIT_COLS;
     const int seg_c1 = min(p.cols, seg_u1 * UNIT_COLS);
     const int scol0 = uit * UNIT_COLS + ls * 128;
@@ -463,13 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           if (valid[j] && ends[j]) mma_commit(bar_d + 8 * (ij[j] % ND));
         ++s_mma;
       }
-      // x for sub-stage s + kNX - 1 reuses the slot of s - 1
-      if (!p.withhold && x_issued < nsub && !*abort_flag) {
-        if (s >= 1) wait(bar_a + 8 * ((s - 1) & 1), (uint32_t)(((s - 1) >> 1) & 1));
-        if (!*abort_flag) issue_x(x_issued++);
-      }
+      // x for sub-stage s + kNX - 2 reuses the slot of s - 2, whose MMAs every
+      // thread saw complete before the barrier above
+      if (!p.withhold && x_issued < nsub && !*abort_flag) issue_x();
       // weights for unit ui + kNW - 1 reuse the slot of ui - 1 (read before the barrier above)
-      if (ls == 0 && w_issued < nunits && !*abort_flag) issue_w(w_issued++);
+      if (ls == 0 && w_issued < nunits && !*abort_flag) issue_w();
     }
 
     // ---- epilogue of the instances that ended in the previous sub-stage
@@ -499,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
 
     // ---- end of a segment: finish it and write y (directly, or through the
     // split-K workspace when the tile is shared with other CTAs)
-    const bool seg_end = ls == SUBS - 1 && (ug + 1 == u_end || (ug + 1) / U != tile);
+    const bool seg_end = ls == SUBS - 1 && (ui + 1 == nunits || uit + 1 == U);
     if (seg_end) {
 #pragma unroll
       for (int i = 0; i < 2; ++i)
