@@ -202,6 +202,30 @@ int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
 int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
                     void* const* y_devs, int m, void* stream);
 
+/*
+ * sgemv_run for 2 <= m <= min(64, max_m) that allocates nothing (the paper
+ * has no counterpart: this is a deployment variant).  Meant for callers
+ * that may not allocate device memory when they run the product: code under
+ * an allocator that owns all device memory (an arena reserved at start-up,
+ * a framework that must account for every byte) and plug-ins handed their
+ * buffers but no right to allocate.  The product, arguments and result are
+ * those of sgemv_run; the difference is where the batch kernel's split-K
+ * workspace lives: instead of the handle's own (allocated by sgemv_create
+ * when max_m >= 2), a fixed array inside the library -- 10 MiB of fp32
+ * partial tiles plus 64 KiB of per-tile counters -- that every GPU which
+ * loads the library holds until the process exits.  Limits: at most
+ * 2,097,152 weight rows (16384 row tiles of 128) -> SGEMV_ERR_UNSUPPORTED
+ * beyond; m outside [2, min(64, max_m)] -> SGEMV_ERR_ARG (m = 1 needs no
+ * workspace: use sgemv_run).  The handle may have been created with any
+ * max_m >= 2.  Every call shares the one array per device and each call
+ * clears its counters first: calls that overlap on the GPU race, so order
+ * them on one stream (they may overlap with sgemv_run calls, which use the
+ * handles' own workspaces).  The first call on a device looks up the
+ * array's device address once, with that device current.  Asynchronous on
+ * `stream`, like sgemv_run.
+ */
+int sgemv_run_noalloc(sgemv_t h, const void* x_dev, void* y_dev, int m, void* stream);
+
 /* Synchronise the device, then return and clear the handle's device error
  * word (SGEMV_OK if no kernel reported an error since the last call).  The
  * batch kernel (2 <= m <= 64) reports SGEMV_ERR_TIMEOUT when one of its

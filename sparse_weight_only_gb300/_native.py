@@ -41,6 +41,7 @@ SIGNATURES = {
     "sgemv_run": (_I, [_P, _P, _P, _I, _P]),
     "sgemv_run_host": (_I, [_P, _P, _P, _I, _P]),
     "sgemv_run_group": (_I, [_P, _I, _P, _P, _I, _P]),
+    "sgemv_run_noalloc": (_I, [_P, _P, _P, _I, _P]),
     "sgemv_status": (_I, [_P]),
     "sgemv_debug_withhold": (_I, [_P, _I]),
     "sgemv_sizes": (_I, [_P, _PSZ, _PSZ, _PSZ, _PSZ]),
@@ -226,6 +227,14 @@ class SparseGemv:
         m = x.shape[0] if x.dim() == 2 else 1
         _check(load().sgemv_run(self._h, x.data_ptr(), y.data_ptr(), m,
                                 _stream_ptr(stream)), "sgemv_run")
+
+    def run_noalloc(self, x, y, stream=None) -> None:
+        """As run(), for 2 <= m <= min(64, max_m), with the split-K workspace
+        in the library's fixed device array instead of the handle's: the call
+        allocates nothing.  Calls of this kind must not overlap on the GPU."""
+        m = x.shape[0] if x.dim() == 2 else 1
+        _check(load().sgemv_run_noalloc(self._h, x.data_ptr(), y.data_ptr(), m,
+                                        _stream_ptr(stream)), "sgemv_run_noalloc")
 
     def __call__(self, x, stream=None):
         import torch

@@ -164,6 +164,13 @@ const char* sgemv_last_error(void) { return g_err; }
 
 }  // extern "C"
 
+namespace sgemv {
+// Status reporting for the library's other translation units: the same
+// thread-local text that sgemv_last_error returns.
+int report(int code, const char* msg) { return fail(code, "%s", msg); }
+int report_cuda(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+}  // namespace sgemv
+
 // Creates a handle; row_group (host, rows entries) optional.
 static int create_impl(sgemv_t* out, int rows, int cols, int n_keep, int group,
                        const int* row_group, int max_m, int device) {

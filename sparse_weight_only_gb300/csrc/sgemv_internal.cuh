@@ -130,6 +130,13 @@ int tc_tiles(const Layout& L);
 bool tc_encode_weights(const Layout& L, const uint4* vals, const uint2* idx, const uint32_t* sz,
                        TcMaps* maps);
 cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s);
+// ... on at most max_ctas CTAs (a workspace sized for that many).
+cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s,
+                      int max_ctas);
+// Sets the calling thread's sgemv_last_error text; returns `code`
+// (report_cuda: SGEMV_ERR_CUDA with the runtime's message).
+int report(int code, const char* msg);
+int report_cuda(cudaError_t e, const char* what);
 // Whether a product of m rows on this layout runs a kernel with the bounded
 // split-K wait that the failure-detection hook can make run out.
 bool withhold_applies(const Layout& L, int m);

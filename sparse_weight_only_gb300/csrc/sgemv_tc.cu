@@ -674,7 +674,8 @@ size_t tc_smem(int npad) {
 }
 
 template <int N, int NPAD>
-cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s) {
+cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s,
+                        int max_ctas) {
   constexpr int UNIT_COLS = N == 2 ? 256 : 512;
   const int sms = tc_sms();
   if (sms <= 0) return cudaErrorNotSupported;
@@ -699,7 +700,8 @@ cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, c
   p.ntiles = (L.rows + kRows - 1) / kRows;
   p.units_per_tile = (L.cols + UNIT_COLS - 1) / UNIT_COLS;
   p.total_units = (long long)p.ntiles * p.units_per_tile;
-  p.grid = (int)(p.total_units < sms ? p.total_units : sms);
+  const int cap = sms < max_ctas ? sms : max_ctas;
+  p.grid = (int)(p.total_units < cap ? p.total_units : cap);
   p.withhold = a.withhold;
   p.wait_ns = a.withhold ? kInjectWaitNs : kWaitLimitNs;
   const size_t smem = tc_smem(NPAD);
@@ -750,6 +752,12 @@ bool tc_encode_weights(const Layout& L, const uint4* vals, const uint2* idx, con
 }
 
 cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s) {
+  return launch_tc(L, a, maps, s, 1 << 30);
+}
+
+cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s,
+                      int max_ctas) {
+  if (max_ctas < 1) return cudaErrorInvalidValue;
   if (a.m < 2 || a.m > 64 || L.rows == 0 || L.cols == 0 || !maps.ready || !maps.scratch ||
       !maps.counters)
     return cudaErrorNotSupported;
@@ -757,17 +765,17 @@ cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cud
   const int np = npad_of(a.m);
   if (L.n_keep == 2) {
     switch (np) {
-      case 16: return launch_tc_n<2, 16>(L, a, maps, s);
-      case 32: return launch_tc_n<2, 32>(L, a, maps, s);
-      case 48: return launch_tc_n<2, 48>(L, a, maps, s);
-      default: return launch_tc_n<2, 64>(L, a, maps, s);
+      case 16: return launch_tc_n<2, 16>(L, a, maps, s, max_ctas);
+      case 32: return launch_tc_n<2, 32>(L, a, maps, s, max_ctas);
+      case 48: return launch_tc_n<2, 48>(L, a, maps, s, max_ctas);
+      default: return launch_tc_n<2, 64>(L, a, maps, s, max_ctas);
     }
   }
   switch (np) {
-    case 16: return launch_tc_n<1, 16>(L, a, maps, s);
-    case 32: return launch_tc_n<1, 32>(L, a, maps, s);
-    case 48: return launch_tc_n<1, 48>(L, a, maps, s);
-    default: return launch_tc_n<1, 64>(L, a, maps, s);
+    case 16: return launch_tc_n<1, 16>(L, a, maps, s, max_ctas);
+    case 32: return launch_tc_n<1, 32>(L, a, maps, s, max_ctas);
+    case 48: return launch_tc_n<1, 48>(L, a, maps, s, max_ctas);
+    default: return launch_tc_n<1, 64>(L, a, maps, s, max_ctas);
   }
 }
 
