@@ -185,10 +185,12 @@ int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
  * projections of a decoder layer, or its gate and up projections -- as
  * y_i = W_hat_i . x for i < count.  This is the grouped run of the
  * layer's decode step (the paper's kernel serves every linear layer of the
- * decode, section 1 contribution 2): with m = 1 the matrices of each N go
- * into one launch that stages x and its lookup tables once per CTA for all
- * of them (at most 8 per launch, more launches beyond that); with m > 1 each
- * matrix runs as in sgemv_run.
+ * decode, section 1 contribution 2): with m = 1 the matrices go into one
+ * launch -- at most 8 of each N; the CTAs of one part take the 2:4 matrices
+ * and those of the other the 1:4 ones, in proportion to their packed bytes,
+ * and each CTA stages x and its lookup table once for all of its matrices
+ * (more than 8 of one N: one launch per N and per 8); with m > 1 each matrix
+ * runs as in sgemv_run.
  *   handles : count packed handles on one device, all with the same cols;
  *             n_keep and group may differ;
  *   x_dev   : m x cols binary16, 16-byte aligned, shared by all;

@@ -562,8 +562,45 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
       if (int rc = run_checked(handles[i], x_dev, y_devs[i], m, s)) return rc;
     return SGEMV_OK;
   }
-  // m = 1: one launch per N for up to max_group() matrices
+  // m = 1: both N in one launch (two CTA ranges) when each fits a launch
   const int cap = sgemv::max_group();
+  {
+    sgemv::Layout L2[8], L1[8];
+    sgemv::RunArgs a2[8], a1[8];
+    int n2 = 0, n1 = 0;
+    bool fits = true;
+    for (int i = 0; i < count && fits; ++i) {
+      sgemv_t h = handles[i];
+      if (h->L.rows == 0) continue;
+      const bool two = h->L.n_keep == 2;
+      int& k = two ? n2 : n1;
+      if (k == cap) {
+        fits = false;
+        break;
+      }
+      (two ? L2 : L1)[k] = h->L;
+      sgemv::RunArgs& a = (two ? a2 : a1)[k];
+      a.vals = h->d_vals;
+      a.idx = h->d_idx;
+      a.sz = h->d_sz;
+      a.x = static_cast<const __half*>(x_dev);
+      a.y = static_cast<__half*>(y_devs[i]);
+      a.m = 1;
+      a.err = h->d_err;
+      ++k;
+    }
+    if (fits && n2 > 0 && n1 > 0) {
+      cudaError_t e = sgemv::launch_m1_group_dual(L2, a2, n2, L1, a1, n1, s);
+      if (e == cudaErrorNotSupported) {
+        (void)cudaGetLastError();
+        return fail(SGEMV_ERR_UNSUPPORTED,
+                    "a grouped matrix is beyond the product kernels' 32-bit chunk index space");
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "grouped SparseGemv launch");
+      return SGEMV_OK;
+    }
+  }
+  // otherwise one launch per N for up to max_group() matrices
   for (int n = 1; n <= 2; ++n) {
     sgemv::Layout Ls[8];
     sgemv::RunArgs as[8];

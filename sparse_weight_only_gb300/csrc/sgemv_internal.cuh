@@ -123,6 +123,10 @@ cudaError_t launch_m1(const Layout& L, const RunArgs& a, cudaStream_t s);
 cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s);
 // m = 1 over several matrices sharing x, cols and N in one launch.
 cudaError_t launch_m1_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s);
+// m = 1 over 2:4 matrices (L2, n2) and 1:4 matrices (L1, n1) sharing x, in
+// one launch of two CTA ranges.
+cudaError_t launch_m1_group_dual(const Layout* L2, const RunArgs* a2, int n2, const Layout* L1,
+                                 const RunArgs* a1, int n1, cudaStream_t s);
 int max_group();
 // Tensor-core batch kernel (sgemv_tc.cu), 2 <= m <= 64.
 size_t tc_scratch_bytes(int max_m);

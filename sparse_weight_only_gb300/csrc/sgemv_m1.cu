@@ -379,8 +379,10 @@ struct Producer {
   }
 };
 
+// The body of one CTA; `cta` is its index within the launch part that
+// covers these matrices (a launch may hold two parts, one per N).
 template <int N, int MODE>
-__global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
+__device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
   using C = M1Cfg<N>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31;
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   uint32_t magic = 0x4B000000u;  // exponent of 2^23, kept in a register
   asm volatile("" : "+r"(magic));
 
-  const int r0 = blockIdx.x * p.rows_per_cta;
+  const int r0 = cta * p.rows_per_cta;
   const int nr = max(0, min(p.rows, r0 + p.rows_per_cta) - r0);
   const int nrw = warp_nrows(warp, nr);
 
@@ -551,6 +553,25 @@ __global__ void __launch_bounds__(kNT, 1) k_m1(M1Params p) {
   cp_wait<0>();  // no copy outstanding when the CTA retires
 }
 
+template <int N, int MODE>
+__global__ void __launch_bounds__(kNT, 1) k_m1(const __grid_constant__ M1Params p) {
+  m1_body<N, MODE>(p, blockIdx.x);
+}
+
+// Matrices of both N that share x in one launch: CTAs [0, grid_a) run the
+// 2:4 part, the others the 1:4 part; each builds only its own pair table.
+struct M1DualParams {
+  M1Params a, b;
+  int grid_a;
+};
+
+__global__ void __launch_bounds__(kNT, 1) k_m1_dual(const __grid_constant__ M1DualParams p) {
+  if ((int)blockIdx.x < p.grid_a)
+    m1_body<2, kMany>(p.a, blockIdx.x);
+  else
+    m1_body<1, kMany>(p.b, blockIdx.x - p.grid_a);
+}
+
 int g_num_sms[64] = {0};
 
 int num_sms() {
@@ -566,9 +587,11 @@ int num_sms() {
   return g_num_sms[dev];
 }
 
-// One launch over `count` matrices that share x, cols and N (count <= kMaxSeg).
+// The plan of one launch part over `count` matrices that share x, cols and
+// N (count <= kMaxSeg), for `ctas` CTAs: parameters, grid and shared memory.
 template <int N, int MODE>
-cudaError_t launch_m1_n(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s) {
+cudaError_t plan_m1(const Layout* Ls, const RunArgs* as, int count, int ctas, M1Params& p,
+                    int& grid, size_t& smem) {
   using C = M1Cfg<N>;
   const Layout& L0 = Ls[0];
   const int chunks = (int)L0.chunks;
@@ -579,10 +602,11 @@ cudaError_t launch_m1_n(const Layout* Ls, const RunArgs* as, int count, cudaStre
       return cudaErrorNotSupported;
     total_rows += Ls[i].rows;
   }
+  grid = 0;
+  smem = 0;
   if (total_rows == 0) return cudaSuccess;
   if (total_rows >= (1ll << 31)) return cudaErrorNotSupported;
-  const int sms = num_sms();
-  if (sms <= 0) return cudaErrorNotSupported;
+  if (ctas <= 0) return cudaErrorNotSupported;
   const size_t ring = (size_t)kNW * kS * kStage;
   const size_t part_max = 4096;   // rows_per_cta <= 1024 when K is sliced
   const size_t room = kSmemLimit - kTabAlign - ring - part_max;
@@ -591,11 +615,10 @@ cudaError_t launch_m1_n(const Layout* Ls, const RunArgs* as, int count, cudaStre
   const int nslices = (chunks + 32 * max_cpl - 1) / (32 * max_cpl);
   const int cpl = (chunks + 32 * nslices - 1) / (32 * nslices);
   const int rows = (int)total_rows;
-  int rows_per_cta = (rows + sms - 1) / sms;
+  int rows_per_cta = (rows + ctas - 1) / ctas;
   if (nslices > 1 && rows_per_cta > 1024) rows_per_cta = 1024;
-  const int grid = (rows + rows_per_cta - 1) / rows_per_cta;
+  grid = (rows + rows_per_cta - 1) / rows_per_cta;
 
-  M1Params p;
   memset(&p, 0, sizeof p);
   int row_begin = 0;
   for (int i = 0; i < count; ++i) {
@@ -626,14 +649,19 @@ cudaError_t launch_m1_n(const Layout* Ls, const RunArgs* as, int count, cudaStre
   p.nslices = nslices;
 
   const size_t part_bytes = nslices > 1 ? ((size_t)rows_per_cta * 4 + 127) & ~(size_t)127 : 0;
-  const size_t smem = kTabAlign + (size_t)cpl * (C::TAB_PER_CPL + C::X_PER_CPL) + part_bytes + ring;
+  smem = kTabAlign + (size_t)cpl * (C::TAB_PER_CPL + C::X_PER_CPL) + part_bytes + ring;
   if (smem > (size_t)kSmemLimit) return cudaErrorNotSupported;
-  static bool attr_set[64] = {false};
+  return cudaSuccess;
+}
+
+template <typename Kernel, typename Params>
+cudaError_t launch_pdl(Kernel kernel, const Params& p, int grid, size_t smem, cudaStream_t s,
+                       bool (&attr_set)[64]) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_m1<N, MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemLimit);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -647,7 +675,19 @@ cudaError_t launch_m1_n(const Layout* Ls, const RunArgs* as, int count, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_m1<N, MODE>, p);
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// One launch over `count` matrices that share x, cols and N (count <= kMaxSeg).
+template <int N, int MODE>
+cudaError_t launch_m1_n(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s) {
+  M1Params p;
+  int grid;
+  size_t smem;
+  cudaError_t e = plan_m1<N, MODE>(Ls, as, count, num_sms(), p, grid, smem);
+  if (e != cudaSuccess || grid == 0) return e;
+  static bool attr_set[64] = {false};
+  return launch_pdl(k_m1<N, MODE>, p, grid, smem, s, attr_set);
 }
 
 }  // namespace
@@ -667,6 +707,37 @@ cudaError_t launch_m1_group(const Layout* Ls, const RunArgs* as, int count, cuda
       return cudaErrorNotSupported;
   return Ls[0].n_keep == 2 ? launch_m1_n<2, kMany>(Ls, as, count, s)
                            : launch_m1_n<1, kMany>(Ls, as, count, s);
+}
+
+cudaError_t launch_m1_group_dual(const Layout* L2, const RunArgs* a2, int n2, const Layout* L1,
+                                 const RunArgs* a1, int n1, cudaStream_t s) {
+  if (n2 < 1 || n2 > kMaxSeg || n1 < 1 || n1 > kMaxSeg) return cudaErrorNotSupported;
+  for (int i = 0; i < n2; ++i)
+    if (a2[i].m != 1 || L2[i].cols != L2[0].cols || L2[i].n_keep != 2 || L2[i].cols == 0)
+      return cudaErrorNotSupported;
+  for (int i = 0; i < n1; ++i)
+    if (a1[i].m != 1 || L1[i].cols != L2[0].cols || L1[i].n_keep != 1)
+      return cudaErrorNotSupported;
+  const int sms = num_sms();
+  if (sms < 2) return cudaErrorNotSupported;
+  // CTAs in proportion to each part's packed chunks (its weight bytes)
+  double b2 = 0.0, b1 = 0.0;
+  for (int i = 0; i < n2; ++i) b2 += (double)L2[i].rows * L2[i].chunks;
+  for (int i = 0; i < n1; ++i) b1 += (double)L1[i].rows * L1[i].chunks;
+  if (b2 <= 0.0 || b1 <= 0.0) return cudaErrorNotSupported;
+  int c2 = (int)(sms * b2 / (b1 + b2) + 0.5);
+  c2 = c2 < 1 ? 1 : (c2 > sms - 1 ? sms - 1 : c2);
+  M1DualParams p;
+  int g2, g1;
+  size_t s2, s1;
+  cudaError_t e = plan_m1<2, kMany>(L2, a2, n2, c2, p.a, g2, s2);
+  if (e != cudaSuccess) return e;
+  e = plan_m1<1, kMany>(L1, a1, n1, sms - c2, p.b, g1, s1);
+  if (e != cudaSuccess) return e;
+  if (g2 == 0 || g1 == 0) return cudaErrorNotSupported;
+  p.grid_a = g2;
+  static bool attr_set[64] = {false};
+  return launch_pdl(k_m1_dual, p, g2 + g1, s2 > s1 ? s2 : s1, s, attr_set);
 }
 
 int max_group() { return kMaxSeg; }

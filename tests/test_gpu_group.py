@@ -27,11 +27,16 @@ def _ys(mats, m):
             for h, _ in mats]
 
 
-@pytest.mark.parametrize("m,cols", [(1, 1536), (5, 1536), (1, 8192)])
-def test_group_matches_single_and_oracle(native, orc, m, cols):
-    specs = [(300, 1, 256), (129, 2, 128), (64, 1, 128), (1, 2, 64),
-             (257, 1, 64), (33, 2, 64), (200, 2, 256), (96, 1, 128),
-             (70, 2, 128), (5, 1, 64)]          # 10 > 8: two launches per N
+SPECS_MIXED = [(300, 1, 256), (129, 2, 128), (64, 1, 128), (1, 2, 64),
+               (257, 1, 64), (33, 2, 64), (200, 2, 256), (96, 1, 128),
+               (70, 2, 128), (5, 1, 64)]      # 5 of each N: one launch, two CTA ranges
+SPECS_MANY = [(40 + 7 * i, 1, (64, 128, 256)[i % 3]) for i in range(9)] + \
+             [(90, 2, 128), (17, 2, 64)]      # 9 > 8 of one N: a launch per N and per 8
+
+
+@pytest.mark.parametrize("m,cols,specs", [(1, 1536, SPECS_MIXED), (5, 1536, SPECS_MIXED),
+                                          (1, 8192, SPECS_MIXED), (1, 1024, SPECS_MANY)])
+def test_group_matches_single_and_oracle(native, orc, m, cols, specs):
     mats = _mats(native, orc, specs, cols, max_m=8)
     x = torch.from_numpy(synth.activations(41 + m, m, cols)).cuda()
     ys = _ys(mats, m)
