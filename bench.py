@@ -430,7 +430,7 @@ def run_ours(args, rank, world, local):
                    "ms_per_step_min": 1e3 * min(rep_t) / args.steps,
                    "ms_per_step_max": 1e3 * max(rep_t) / args.steps}
     if grouped:
-        per_step = sum(len({gvs[i].n_keep for i in grp}) for grp in groups)
+        per_step = len(groups)      # one launch per group (both N in one launch)
     else:
         per_step = len(gvs)
     launches = per_step * args.steps

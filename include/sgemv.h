@@ -153,10 +153,11 @@ int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
 
 /*
  * y = W_hat . x for m activation rows (0 <= m <= max_m).  m = 1 runs the
- * CUDA-core decode kernel; 2 <= m <= 64 (beam candidates, prefix-tree
- * verification nodes: the paper's parallel verification, section 3.1) runs
- * the sparse tensor-core kernel, with the 2-bit positions as the MMA's 2:4
- * metadata and the accumulators in tensor memory.
+ * CUDA-core decode kernel; batches (beam candidates, prefix-tree
+ * verification nodes: the paper's parallel verification, section 3.1) run
+ * on the sparse tensor cores with the 2-bit positions as the MMA's 2:4
+ * metadata -- 2 <= m <= 16 with the warp-level sparse MMA, 17 <= m <= 64
+ * with tcgen05 and the accumulators in tensor memory.
  *   x_dev : m x cols binary16, row-major, 16-byte aligned, device memory;
  *   y_dev : m x rows binary16, row-major, 2-byte aligned, device memory,
  *           fully overwritten; must not overlap x_dev;
@@ -229,23 +230,29 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
 int sgemv_run_noalloc(sgemv_t h, const void* x_dev, void* y_dev, int m, void* stream);
 
 /* Synchronise the device, then return and clear the handle's device error
- * word (SGEMV_OK if no kernel reported an error since the last call).  The
- * batch kernel (2 <= m <= 64) reports SGEMV_ERR_TIMEOUT when one of its
- * bounded waits -- for its own TMA copies and MMAs -- gave up after about a
- * second: it then stops issuing work, lets the copies it issued land, frees
- * its tensor memory, returns the split-K counters to zero and exits; the
- * outputs of that call are undefined and later calls are unaffected.  No
- * kernel of the library waits on another CTA. */
+ * word (SGEMV_OK if no kernel reported an error since the last call).  A
+ * batch kernel reports SGEMV_ERR_TIMEOUT when one of its bounded waits gave
+ * up after about a second; the outputs of that call are then undefined and
+ * later calls are unaffected.  2 <= m <= 16: the split-K reduction waiting
+ * for the partial sums of the other CTAs of its cluster -- every CTA still
+ * issues all of its sends and no CTA retires before every CTA of its cluster
+ * has issued them, so no late store lands in a retired CTA; what the limit
+ * cannot guard against is a CTA that never reaches its sends (the launch
+ * then does not finish).  17 <= m <= 64: the waits for its own TMA copies
+ * and MMAs -- it then stops issuing work, lets the copies it issued land,
+ * frees its tensor memory and completes its split-K counters. */
 int sgemv_status(sgemv_t h);
 
 /*
  * Failure-detection test hook (not a paper operation).  The next `runs`
- * batch products on this handle (2 <= m <= 64) withhold their x copies and
- * shorten the bounded waits to about 20 microseconds, so the wait for x runs
- * out: sgemv_status then returns SGEMV_ERR_TIMEOUT and y of those calls is
- * undefined.  Nothing the kernel waits for is in flight when it gives up,
- * the device stays usable and later calls run normally.  m = 1 calls do not
- * consume the hook.  runs = 0 cancels; runs < 0 -> SGEMV_ERR_ARG.
+ * batch products on this handle (2 <= m <= 64) make their bounded wait run
+ * out: for 2 <= m <= 16 every cluster rank withholds its split-K partial
+ * sums, for larger m the kernel withholds its x copies, and the wait limit
+ * drops to about 20 microseconds.  sgemv_status then returns
+ * SGEMV_ERR_TIMEOUT and y of those calls is undefined.  Nothing the kernel
+ * waits for is in flight when it gives up, the device stays usable and
+ * later calls run normally.  m = 1 calls do not consume the hook.
+ * runs = 0 cancels; runs < 0 -> SGEMV_ERR_ARG.
  */
 int sgemv_debug_withhold(sgemv_t h, int runs);
 

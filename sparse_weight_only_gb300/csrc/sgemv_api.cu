@@ -447,14 +447,12 @@ static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s)
     CUDA_TRY(cudaMemsetAsync(a.y, 0, (size_t)m * L.rows * sizeof(__half), s), "zero y");
     return SGEMV_OK;
   }
-  // m = 1: the CUDA-core table kernel; m >= 2: the sparse tensor-core kernel
-  // (1:4 as 2:4 with a zero partner per quad)
-#ifdef SGEMV_BATCH_MMA_SYNC
-  // build option: the warp-level mma.sp batch kernel instead of tcgen05
-  cudaError_t e = m == 1 ? sgemv::launch_m1(L, a, s) : sgemv::launch_mma(L, a, s);
-#else
-  cudaError_t e = m == 1 ? sgemv::launch_m1(L, a, s) : sgemv::launch_tc(L, a, h->tc, s);
-#endif
+  // m = 1: the CUDA-core pair-table kernel; 2 <= m <= 16: the warp-level
+  // sparse MMA kernel; 17 <= m <= 64: the tcgen05 kernel (each measured the
+  // fastest in its range on the verification-batch layer set)
+  cudaError_t e = m == 1                       ? sgemv::launch_m1(L, a, s)
+                  : m <= sgemv::kMmaSyncMaxM ? sgemv::launch_mma(L, a, s)
+                                             : sgemv::launch_tc(L, a, h->tc, s);
   if (e == cudaErrorNotSupported) {
     (void)cudaGetLastError();
     return fail(SGEMV_ERR_UNSUPPORTED,

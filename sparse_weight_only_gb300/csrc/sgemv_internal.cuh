@@ -142,7 +142,10 @@ cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cud
 int report(int code, const char* msg);
 int report_cuda(cudaError_t e, const char* what);
 // Whether a product of m rows on this layout runs a kernel with the bounded
-// split-K wait that the failure-detection hook can make run out.
+// waits that the failure-detection hook can make run out.
 bool withhold_applies(const Layout& L, int m);
+// Largest m that the warp-level sparse MMA kernel (sgemv_mma.cu) takes;
+// larger batches run the tcgen05 kernel (sgemv_tc.cu).
+constexpr int kMmaSyncMaxM = 16;
 
 }  // namespace sgemv

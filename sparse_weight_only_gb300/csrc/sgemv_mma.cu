@@ -1,6 +1,8 @@
 // sgemv_mma.cu -- SparseGemv for a small batch of activation rows on the
-// tensor cores: 2 <= m <= 64 (beam candidates / prefix-tree verification
-// nodes), 2:4 weights and 1:4 weights (each kept weight paired with a zero).
+// tensor cores with the warp-level sparse MMA: 2 <= m <= 16 (beam
+// candidates / prefix-tree verification nodes; larger batches run the
+// tcgen05 kernel of sgemv_tc.cu, and this kernel takes any m <= 64), 2:4
+// weights and 1:4 weights (each kept weight paired with a zero).
 //
 // Product (Dong et al., arXiv 2605.11582, section 1 contribution 2 and
 // section 3.3, applied to the verification batch of section 3.1):
@@ -643,12 +645,9 @@ int g_sms[64] = {0};
 }  // namespace
 
 bool withhold_applies(const Layout& L, int m) {
-#ifdef SGEMV_BATCH_MMA_SYNC
-  return m >= 2 && push_reduce((m + 7) / 8) && L.rows > 0 && L.cols > 0;
-#else
-  // the tensor-core kernel's x loads (every batch size)
+  // m <= 16: this kernel's pushed split-K sums; larger m: the tcgen05
+  // kernel's x copies
   return m >= 2 && L.rows > 0 && L.cols > 0;
-#endif
 }
 
 cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s) {

@@ -47,12 +47,11 @@
 namespace sgemv {
 namespace {
 
-constexpr int kThreads = 256;          // 8 warps: lane quadrant w % 4, k-step half w / 4
+constexpr int kThreads = 480;          // 15 warps: 8 decode, 4 epilogue, 2 MMA issue, TMA producer
 constexpr int kRows = 128;             // weight rows per tile (MMA M)
 constexpr int kNW = 6;                 // weight units in the shared-memory ring
 constexpr int kNX = 6;                 // x sub-stages in the ring (refilled 2 behind)
 constexpr int kTmemCols = 512;
-constexpr int kDCols = 256;            // accumulator blocks live in columns [0, 256)
 // one weight unit: codes 128 rows x 64 B (64-byte swizzle) | positions
 // 128 x 32 B (32-byte swizzle) | scale/zero words 128 x 32 B
 constexpr int kStageW = 16384;
@@ -93,6 +92,20 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+// Non-blocking test (try_wait may suspend the thread for a while): for a
+// thread that polls several barriers in turn.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -213,15 +226,77 @@ __device__ __forceinline__ uint32_t meta_lane(uint32_t mw, int lane) {
 // (tile, unit) order; each unit is SUBS sub-stages of four 32-column
 // k-steps.  A "segment" is the CTA's run of units inside one tile; a group
 // "instance" is a maximal run of the segment's k-steps inside one
-// quantisation group and owns one accumulator block.
+// quantisation group inside one sub-stage and owns one accumulator block.
+// Every role walks the same sequence; they meet only at mbarriers:
+//   producer (warp 14)  --weights-->  decode warps 0-7  --A, metadata-->
+//   MMA warps 12, 13  --accumulator blocks-->  epilogue warps 8-11  --y
+// Weight units have a full and an empty barrier, x sub-stages and A slots a
+// full one; a single MMA commit per sub-stage ("sub-stage done") frees its
+// A slot and x slot and finalises its accumulator blocks; the epilogue
+// frees each block for reuse.
+
+// The walk over the CTA's units: position (tile, unit in tile) stepped
+// forward in 32-bit arithmetic, and the segment bounds.
+struct Walk {
+  int U, nunits;
+  int tile, uit, seg_u0;
+  __device__ __forceinline__ Walk(int U_, int nunits_, int tile0, int uit0)
+      : U(U_), nunits(nunits_), tile(tile0), uit(uit0), seg_u0(uit0) {}
+  // call at the first sub-stage of unit ui > 0
+  __device__ __forceinline__ void next_unit() {
+    if (++uit == U) {
+      uit = 0;
+      ++tile;
+      seg_u0 = 0;
+    }
+  }
+  __device__ __forceinline__ int seg_u1(int ui) const { return min(U, uit + (nunits - ui)); }
+  __device__ __forceinline__ bool unit_ends_segment(int ui) const {
+    return ui + 1 == nunits || uit + 1 == U;
+  }
+};
+
+// The k-steps of one sub-stage: which are inside K, which start and end a
+// group instance, and the instance each belongs to.  An instance never
+// spans two sub-stages (a 256-column group is two instances, each scaled
+// by the group's scale), so every sub-stage's MMAs stand alone.
+struct Steps {
+  int ij[4];
+  bool valid[4], first[4], ends[4];
+  __device__ __forceinline__ void walk(int scol0, int seg_c1, int group, int& inst) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = scol0 + 32 * j;
+      valid[j] = col < seg_c1;
+      first[j] = false;
+      ends[j] = false;
+      if (valid[j]) {
+        if (j == 0 || (col & (group - 1)) == 0) {
+          ++inst;
+          first[j] = true;
+        }
+        ends[j] = j == 3 || col + 32 >= seg_c1 || ((col + 32) & (group - 1)) == 0;
+      }
+      ij[j] = inst;
+    }
+  }
+};
+
+constexpr int kDecodeWarps = 8;
+constexpr int kEpiWarp0 = 8;           // epilogue warps 8..11 (lane quadrant w - 8)
+constexpr int kMmaWarp = 12;           // MMA issue: warps 12 and 13, alternate sub-stages
+constexpr int kProdWarp = 14;
+constexpr int kRD = 32;                // "sub-stage done" barriers (ring)
+
 template <int N, int NPAD>
 __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcParams p) {
   constexpr int SUBS = N == 2 ? 2 : 4;           // sub-stages per unit
   constexpr int UNIT_COLS = 128 * SUBS;          // 256 or 512 dense columns
   constexpr int XBOX = NPAD * 128;               // bytes of one 64-column x tile
   constexpr int XSUB = 2 * XBOX;
-  constexpr int ND = kDCols / NPAD;              // accumulator blocks
-  constexpr int HALF = NPAD / 2;                 // accumulator columns per thread
+  constexpr int DCOLS = NPAD <= 32 ? 128 : 256;  // accumulator region of tensor memory
+  constexpr int ND = DCOLS / NPAD;               // accumulator blocks
+  constexpr int NA = (kTmemCols - DCOLS) / 128;  // A/metadata slots (sub-stages)
   constexpr uint32_t IDESC = (1u << 2) | (1u << 4) | ((uint32_t)(NPAD >> 3) << 17) |
                              ((uint32_t)(kRows >> 4) << 24);
 
@@ -232,19 +307,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   const uint32_t wring = base;
   const uint32_t xring = base + kNW * kStageW;
   const uint32_t bars = xring + kNX * XSUB;
-  const uint32_t bar_w = bars;                    // kNW  weight unit landed
-  const uint32_t bar_x = bars + 8 * kNW;          // kNX  x sub-stage landed
-  const uint32_t bar_a = bar_x + 8 * kNX;         // 2    MMAs of an A/metadata slot done
-  const uint32_t bar_d = bar_a + 16;              // ND   accumulator block ready
-  const uint32_t misc = bar_d + 8 * ND;           // tmem base, abort flag, last-arriver flag
+  // weight unit full / empty; x sub-stage full; A/metadata slot full; the
+  // "sub-stage done" ring (one MMA commit per sub-stage: its A slot, x slot
+  // and accumulator blocks are then free / final); accumulator block empty
+  const uint32_t bar_wf = bars, bar_we = bar_wf + 8 * kNW;
+  const uint32_t bar_xf = bar_we + 8 * kNW;
+  const uint32_t bar_af = bar_xf + 8 * kNX;
+  const uint32_t bar_dn = bar_af + 8 * NA;
+  const uint32_t bar_de = bar_dn + 8 * kRD;
+  const uint32_t misc = bar_de + 8 * ND;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + (misc - base));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + (misc - base) + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(sm + (misc - base) + 8);
+  volatile int* pub = reinterpret_cast<volatile int*>(sm + (misc - base) + 12);  // w, x, mma ends
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, h = warp >> 2;
-  const int r = quad * 32 + lane;                 // this thread's row of the tile
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
 
   const int U = p.units_per_tile;
   const long long T = p.total_units;
@@ -253,17 +330,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   const long long u_end = (long long)(blockIdx.x + 1) * T / P;
   const int nunits = (int)(u_end - u_begin);
   const int nsub = nunits * SUBS;
+  const int tile0 = (int)(u_begin / U), uit0 = (int)(u_begin % U);
 
   if (tid == 0) {
-    for (int i = 0; i < kNW; ++i) mbar_init(bar_w + 8 * i, 1);
-    for (int i = 0; i < kNX; ++i) mbar_init(bar_x + 8 * i, 1);
-    mbar_init(bar_a, 1);
-    mbar_init(bar_a + 8, 1);
-    for (int i = 0; i < ND; ++i) mbar_init(bar_d + 8 * i, 1);
+    for (int i = 0; i < kNW; ++i) {
+      mbar_init(bar_wf + 8 * i, 1);
+      mbar_init(bar_we + 8 * i, kDecodeWarps + 4);
+    }
+    for (int i = 0; i < kNX; ++i) mbar_init(bar_xf + 8 * i, 1);
+    for (int i = 0; i < NA; ++i) mbar_init(bar_af + 8 * i, kDecodeWarps);
+    for (int i = 0; i < kRD; ++i) mbar_init(bar_dn + 8 * i, 1);
+    for (int i = 0; i < ND; ++i) mbar_init(bar_de + 8 * i, 4);
     *abort_flag = 0;
+    pub[0] = pub[1] = pub[2] = pub[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(misc),
                  "n"(kTmemCols)
                  : "memory");
@@ -274,44 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // (tile, unit in tile) of the CTA's first unit: one 64-bit division here,
-  // then every walk over the units steps these forward in 32-bit arithmetic
-  const int tile0 = (int)(u_begin / U), uit0 = (int)(u_begin % U);
-
-  // ---- producer state (thread 0): the next weight unit and x sub-stage to
-  // load, each with its own (tile, unit) position
-  int w_issued = 0, x_issued = 0;
-  int w_tile = tile0, w_uit = uit0;
-  int x_uit = uit0, x_ls = 0;
-  auto issue_w = [&]() {   // weight unit w_issued into slot w_issued % kNW
-    const uint32_t dst = wring + (uint32_t)((w_issued % kNW) * kStageW);
-    const uint32_t bar = bar_w + 8 * (w_issued % kNW);
-    mbar_expect_tx(bar, kStageW);
-    const int chunk0 = w_uit * 4;
-    const int g0 = ((w_uit * UNIT_COLS) >> p.gshift) & ~3;
-    tma_2d(dst + kValsOff, &p.tm_vals, chunk0 * 16, w_tile * kRows, bar);
-    tma_2d(dst + kIdxOff, &p.tm_idx, chunk0 * 8, w_tile * kRows, bar);
-    tma_2d(dst + kSzOff, &p.tm_sz, g0, w_tile * kRows, bar);
-    ++w_issued;
-    if (++w_uit == U) {
-      w_uit = 0;
-      ++w_tile;
-    }
-  };
-  auto issue_x = [&]() {   // x of sub-stage x_issued into slot x_issued % kNX
-    const int col0 = x_uit * UNIT_COLS + x_ls * 128;
-    const uint32_t dst = xring + (uint32_t)((x_issued % kNX) * XSUB);
-    const uint32_t bar = bar_x + 8 * (x_issued % kNX);
-    mbar_expect_tx(bar, XSUB);
-    tma_2d(dst, &p.tm_x, col0, 0, bar);
-    tma_2d(dst + XBOX, &p.tm_x, col0 + 64, 0, bar);
-    ++x_issued;
-    if (++x_ls == SUBS) {
-      x_ls = 0;
-      if (++x_uit == U) x_uit = 0;
-    }
-  };
-  // bounded wait: false when it ran out (abort set) or another thread aborted
+  // bounded wait: false when it ran out (then abort is set) or another role aborted
   auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
@@ -326,256 +371,297 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     return true;
   };
 
-  if (tid == 0)
-    while (w_issued < min(nunits, kNW - 1)) issue_w();
-  // x and the split-K workspace may be in use by the previous kernel
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
-  if (tid == 0 && !p.withhold)
-    while (x_issued < min(nsub, kNX - 2)) issue_x();
-
-  float acc[HALF];
-#pragma unroll
-  for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
-  // instances that ended in the previous sub-stage: block and this row's scale
-  int pend_n = 0;
-  int pend_blk[2] = {0, 0};
-  uint32_t pend_par[2] = {0, 0};
-  float pend_s[2] = {0.0f, 0.0f};
-  int inst = -1;                   // instance index of the CTA (block = inst % ND)
-  bool first_seg = true;
-  int tile = tile0, uit = uit0;    // position of the current unit
-  int seg_u0 = uit0;               // first unit of the current segment in its tile
-
-  // epilogue of one finished instance: acc += s * D[block]
-  auto drain = [&](int blk, uint32_t par, float s) {
-    wait(bar_d + 8 * blk, par);
-    fence_after();
-    const uint32_t taddr = tmem + lane_off + (uint32_t)(blk * NPAD + h * HALF);
-    uint32_t v[HALF];
-#pragma unroll
-    for (int c8 = 0; c8 < HALF / 8; ++c8) {
-      uint32_t (&v8)[8] = *reinterpret_cast<uint32_t (*)[8]>(v + 8 * c8);
-      ld8(taddr + 8 * c8, v8);
-    }
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < HALF; ++i) acc[i] = fmaf(s, __uint_as_float(v[i]), acc[i]);
-  };
-  // split-K arrivals of this CTA's partial segments (the first and the last)
-  bool counted[2] = {false, false};
-  int s_mma = 0;   // sub-stages whose MMAs thread 0 issued
-
-  for (int s = 0; s < nsub; ++s) {
-    const int ui = s / SUBS, ls = s % SUBS;
-    if (ls == 0 && ui > 0 && ++uit == U) {   // next unit; a new tile starts a segment
-      uit = 0;
-      ++tile;
-      seg_u0 = 0;
-    }
-    const int seg_u1 = min(U, uit + (nunits - ui));   // the segment's units end
-    const int seg_c0 = seg_u0 * UNIT_COLS;
-    const int seg_c1 = min(p.cols, seg_u1 * UNIT_COLS);
-    const int scol0 = uit * UNIT_COLS + ls * 128;
-    const uint32_t wslot = wring + (uint32_t)((ui % kNW) * kStageW);
-    const int t = s & 1;
-
-    if (ls == 0) wait(bar_w + 8 * (ui % kNW), (uint32_t)((ui / kNW) & 1));
-
-    // ---- decode this thread's two k-steps (2h, 2h + 1) of the sub-stage
-    const int g0 = ((uit * UNIT_COLS) >> p.gshift) & ~3;
-    const int myG = (scol0 + 64 * h) >> p.gshift;
-    const uint32_t szw = lds32(wslot + kSzOff + (uint32_t)(r * 32 + (myG - g0) * 4));
-    uint32_t a0[8], a1[8];
-    uint32_t m0, m1;
-    if constexpr (N == 2) {
-      const int ch = 2 * ls + h;                              // chunk of the unit
-      const uint4 v = lds128(wslot + kValsOff + (uint32_t)(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
-      const uint2 ix = lds64(wslot + kIdxOff +
-                             (uint32_t)(r * 32 + ((ls ^ ((r >> 2) & 1)) << 4) + h * 8));
-      const uint32_t zc = zconst(szw);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        a0[c] = quad24(c < 4 ? v.x : v.y, c & 3, zc);
-        a1[c] = quad24(c < 4 ? v.z : v.w, c & 3, zc);
-      }
-      m0 = ix.x;
-      m1 = ix.y;
-    } else {
-      const uint2 v = lds64(wslot + kValsOff +
-                            (uint32_t)(r * 64 + ((ls ^ ((r >> 1) & 3)) << 4) + h * 8));
-      const uint32_t pw = lds32(wslot + kIdxOff +
-                                (uint32_t)(r * 32 + (((ls >> 1) ^ ((r >> 2) & 1)) << 4) +
-                                           (ls & 1) * 8 + h * 4));
-      const uint32_t z1024 = __byte_perm(zconst(szw), 0u, 0x1010u);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        quads14(v.x, c, pw, z1024, a0[c], a0[c + 4]);
-        quads14(v.y, c, pw >> 16, z1024, a1[c], a1[c + 4]);
-      }
-      m0 = meta14(pw & 0xFFFFu);
-      m1 = meta14(pw >> 16);
-    }
-    m0 = meta_lane(m0, lane);
-    m1 = meta_lane(m1, lane);
-
-    // ---- into the A / metadata slot t (free once the MMAs of s - 2 are done)
-    if (s >= 2) wait(bar_a + 8 * t, (uint32_t)(((s - 2) >> 1) & 1));
-    fence_after();
-    const uint32_t slot_col = (uint32_t)(kDCols + 32 * (4 * t + 2 * h));
-    st8(tmem + lane_off + slot_col + 8, a0);
-    st8(tmem + lane_off + slot_col + 32 + 8, a1);
-    st1(tmem + lane_off + slot_col, m0);
-    st1(tmem + lane_off + slot_col + 32, m1);
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-    fence_before();
-    __syncthreads();
-    const bool aborted = *abort_flag != 0;
-    if (aborted) break;
-
-    // ---- instances of this sub-stage (the same walk in every thread)
-    int ij[4];
-    uint32_t first[4];
-    bool valid[4], ends[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int col = scol0 + 32 * j;
-      valid[j] = col < seg_c1;
-      first[j] = 0;
-      ends[j] = false;
-      if (valid[j]) {
-        if (col == seg_c0 || (col & (p.group - 1)) == 0) {
-          ++inst;
-          first[j] = 1;
+  if (warp == kProdWarp) {
+    // ======================= producer: TMA copies =========================
+    if (lane == 0) {
+      int w_issued = 0, x_issued = 0;
+      int w_tile = tile0, w_uit = uit0, x_uit = uit0, x_ls = 0;
+      auto issue_w = [&]() {
+        const uint32_t dst = wring + (uint32_t)((w_issued % kNW) * kStageW);
+        const uint32_t bar = bar_wf + 8 * (w_issued % kNW);
+        mbar_expect_tx(bar, kStageW);
+        const int chunk0 = w_uit * 4;
+        const int g0 = ((w_uit * UNIT_COLS) >> p.gshift) & ~3;
+        tma_2d(dst + kValsOff, &p.tm_vals, chunk0 * 16, w_tile * kRows, bar);
+        tma_2d(dst + kIdxOff, &p.tm_idx, chunk0 * 8, w_tile * kRows, bar);
+        tma_2d(dst + kSzOff, &p.tm_sz, g0, w_tile * kRows, bar);
+        ++w_issued;
+        if (++w_uit == U) {
+          w_uit = 0;
+          ++w_tile;
         }
-        ends[j] = col + 32 >= seg_c1 || ((col + 32) & (p.group - 1)) == 0;
+      };
+      auto issue_x = [&]() {
+        const int col0 = x_uit * UNIT_COLS + x_ls * 128;
+        const uint32_t dst = xring + (uint32_t)((x_issued % kNX) * XSUB);
+        const uint32_t bar = bar_xf + 8 * (x_issued % kNX);
+        mbar_expect_tx(bar, XSUB);
+        tma_2d(dst, &p.tm_x, col0, 0, bar);
+        tma_2d(dst + XBOX, &p.tm_x, col0 + 64, 0, bar);
+        ++x_issued;
+        if (++x_ls == SUBS) {
+          x_ls = 0;
+          if (++x_uit == U) x_uit = 0;
+        }
+      };
+      // the weights do not depend on the previous kernel: in flight before the wait
+      while (w_issued < min(nunits, kNW)) issue_w();
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      const int x_total = p.withhold ? 0 : nsub;
+      unsigned long long t0 = global_ns();
+      while ((w_issued < nunits || x_issued < x_total) && !*abort_flag) {
+        bool moved = false;
+        if (x_issued < x_total &&
+            (x_issued < kNX || mbar_test(bar_dn + 8 * ((x_issued - kNX) % kRD),
+                                         (uint32_t)(((x_issued - kNX) / kRD) & 1)))) {
+          issue_x();
+          moved = true;
+        }
+        if (w_issued < nunits &&
+            mbar_test(bar_we + 8 * (w_issued % kNW), (uint32_t)(((w_issued / kNW) - 1) & 1))) {
+          issue_w();
+          moved = true;
+        }
+        if (moved) {
+          t0 = global_ns();
+        } else if (global_ns() - t0 > p.wait_ns) {
+          *abort_flag = 1;
+          atomicCAS(p.err, 0, kDevErrTimeout);
+        }
       }
-      ij[j] = inst;
+      pub[0] = w_issued;
+      pub[1] = x_issued;
     }
+  } else {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
+  asm volatile("griddepcontrol.launch_dependents;");
 
-    // ---- thread 0: the MMAs of this sub-stage and the loads ahead
-    if (tid == 0) {
+  if (warp < kDecodeWarps) {
+    // ======================= decode: weights -> A, metadata ===============
+    const int quad = warp & 3, h = warp >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    int uit = uit0;
+    for (int s = 0; s < nsub; ++s) {
+      const int ui = s / SUBS, ls = s % SUBS;
+      if (ls == 0 && ui > 0 && ++uit == U) uit = 0;
+      const uint32_t wslot = wring + (uint32_t)((ui % kNW) * kStageW);
+      if (ls == 0 && !__all_sync(0xffffffffu, wait(bar_wf + 8 * (ui % kNW), (uint32_t)((ui / kNW) & 1))))
+        break;
+      const int scol0 = uit * UNIT_COLS + ls * 128;
+      const int g0 = ((uit * UNIT_COLS) >> p.gshift) & ~3;
+      const int myG = (scol0 + 64 * h) >> p.gshift;
+      const uint32_t szw = lds32(wslot + kSzOff + (uint32_t)(r * 32 + (myG - g0) * 4));
+      uint32_t a0[8], a1[8];
+      uint32_t m0, m1;
+      if constexpr (N == 2) {
+        const int ch = 2 * ls + h;
+        const uint4 v = lds128(wslot + kValsOff + (uint32_t)(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
+        const uint2 ix = lds64(wslot + kIdxOff +
+                               (uint32_t)(r * 32 + ((ls ^ ((r >> 2) & 1)) << 4) + h * 8));
+        const uint32_t zc = zconst(szw);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          a0[c] = quad24(c < 4 ? v.x : v.y, c & 3, zc);
+          a1[c] = quad24(c < 4 ? v.z : v.w, c & 3, zc);
+        }
+        m0 = ix.x;
+        m1 = ix.y;
+      } else {
+        const uint2 v = lds64(wslot + kValsOff +
+                              (uint32_t)(r * 64 + ((ls ^ ((r >> 1) & 3)) << 4) + h * 8));
+        const uint32_t pw = lds32(wslot + kIdxOff +
+                                  (uint32_t)(r * 32 + (((ls >> 1) ^ ((r >> 2) & 1)) << 4) +
+                                             (ls & 1) * 8 + h * 4));
+        const uint32_t z1024 = __byte_perm(zconst(szw), 0u, 0x1010u);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          quads14(v.x, c, pw, z1024, a0[c], a0[c + 4]);
+          quads14(v.y, c, pw >> 16, z1024, a1[c], a1[c + 4]);
+        }
+        m0 = meta14(pw & 0xFFFFu);
+        m1 = meta14(pw >> 16);
+      }
+      m0 = meta_lane(m0, lane);
+      m1 = meta_lane(m1, lane);
+      if (ls == SUBS - 1) {   // this warp is done with the unit's shared memory
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_we + 8 * (ui % kNW));
+      }
+      // the A/metadata slot of s is free once the MMAs of s - NA are done
+      const int t = s % NA;
+      if (s >= NA && !__all_sync(0xffffffffu, wait(bar_dn + 8 * ((s - NA) % kRD),
+                                                    (uint32_t)(((s - NA) / kRD) & 1))))
+        break;
       fence_after();
-      if (wait(bar_x + 8 * (s % kNX), (uint32_t)((s / kNX) & 1))) {
+      const uint32_t slot_col = (uint32_t)(DCOLS + 32 * (4 * t + 2 * h));
+      st8(tmem + lane_off + slot_col + 8, a0);
+      st8(tmem + lane_off + slot_col + 32 + 8, a1);
+      st1(tmem + lane_off + slot_col, m0);
+      st1(tmem + lane_off + slot_col + 32, m1);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_af + 8 * t);
+    }
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ======================= MMA issue ====================================
+    // Two threads in two warps take alternate sub-stages (a sub-stage's MMAs
+    // stand alone: its own A slot, x slot and accumulator blocks).
+    if (lane == 0) {
+      const int mine = warp - kMmaWarp;
+      Walk wk(U, nunits, tile0, uit0);
+      int inst = -1, s_end = 0;
+      for (int s = 0; s < nsub && !*abort_flag; ++s) {
+        const int ui = s / SUBS, ls = s % SUBS;
+        if (ls == 0 && ui > 0) wk.next_unit();
+        const int seg_c1 = min(p.cols, wk.seg_u1(ui) * UNIT_COLS);
+        Steps st;
+        st.walk(wk.uit * UNIT_COLS + ls * 128, seg_c1, p.group, inst);
+        if ((s & 1) != mine) continue;
+        const int t = s % NA;
+        if (!wait(bar_af + 8 * t, (uint32_t)((s / NA) & 1))) break;
+        if (!wait(bar_xf + 8 * (s % kNX), (uint32_t)((s / kNX) & 1))) break;
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (st.valid[j] && st.first[j] && st.ij[j] >= ND)
+            ok = ok && wait(bar_de + 8 * (st.ij[j] % ND), (uint32_t)(((st.ij[j] / ND) - 1) & 1));
+        if (!ok) break;
+        fence_after();
         const uint32_t xb = xring + (uint32_t)((s % kNX) * XSUB);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (!valid[j]) continue;
-          const uint32_t col = (uint32_t)(kDCols + 32 * (4 * t + j));
-          mma_sp(tmem + (uint32_t)((ij[j] % ND) * NPAD), tmem + col + 8,
+          if (!st.valid[j]) continue;
+          const uint32_t col = (uint32_t)(DCOLS + 32 * (4 * t + j));
+          mma_sp(tmem + (uint32_t)((st.ij[j] % ND) * NPAD), tmem + col + 8,
                  desc_sw128(xb + (uint32_t)((j >> 1) * XBOX + (j & 1) * 64)), tmem + col, IDESC,
-                 first[j] ? 0u : 1u);
+                 st.first[j] ? 0u : 1u);
         }
-        mma_commit(bar_a + 8 * t);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (valid[j] && ends[j]) mma_commit(bar_d + 8 * (ij[j] % ND));
-        ++s_mma;
+        mma_commit(bar_dn + 8 * (s % kRD));
+        s_end = s + 1;
       }
-      // x for sub-stage s + kNX - 2 reuses the slot of s - 2, whose MMAs every
-      // thread saw complete before the barrier above
-      if (!p.withhold && x_issued < nsub && !*abort_flag) issue_x();
-      // weights for unit ui + kNW - 1 reuse the slot of ui - 1 (read before the barrier above)
-      if (ls == 0 && w_issued < nunits && !*abort_flag) issue_w();
+      pub[2 + mine] = s_end;
     }
-
-    // ---- epilogue of the instances that ended in the previous sub-stage
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+    // ======================= epilogue: accumulators -> y ==================
+    // Each thread owns one row; its warps never leave the walk early (a wait
+    // that runs out just skips ahead), so the named barrier of the split-K
+    // hand-off and the per-tile counters always see every epilogue thread.
+    const int quad = warp - kEpiWarp0;
+    const int r = quad * 32 + lane;
+    const int etid = tid - 32 * kEpiWarp0;       // 0..127
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    Walk wk(U, nunits, tile0, uit0);
+    int inst = -1;
+    bool first_seg = true;
+    float acc[NPAD];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if (i < pend_n) drain(pend_blk[i], pend_par[i], pend_s[i]);
-    pend_n = 0;
-    // instances ending here: block, phase and this row's scale (at most two)
+    for (int i = 0; i < NPAD; ++i) acc[i] = 0.0f;
+    for (int s = 0; s < nsub; ++s) {
+      const int ui = s / SUBS, ls = s % SUBS;
+      if (ls == 0 && ui > 0) wk.next_unit();
+      const int seg_u1 = wk.seg_u1(ui);
+      const int seg_c1 = min(p.cols, seg_u1 * UNIT_COLS);
+      const int scol0 = wk.uit * UNIT_COLS + ls * 128;
+      const uint32_t wslot = wring + (uint32_t)((ui % kNW) * kStageW);
+      const int g0 = ((wk.uit * UNIT_COLS) >> p.gshift) & ~3;
+      Steps st;
+      st.walk(scol0, seg_c1, p.group, inst);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (valid[j] && ends[j]) {
+      for (int j = 0; j < 4; ++j) {
+        if (!(st.valid[j] && st.ends[j])) continue;
+        const int blk = st.ij[j] % ND;
+        __all_sync(0xffffffffu, wait(bar_dn + 8 * (s % kRD), (uint32_t)((s / kRD) & 1)));
+        fence_after();
         const int G = (scol0 + 32 * j) >> p.gshift;
         const uint32_t w = lds32(wslot + kSzOff + (uint32_t)(r * 32 + (G - g0) * 4));
         const float sc = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
-        if (pend_n == 0) {
-          pend_blk[0] = ij[j] % ND;
-          pend_par[0] = (uint32_t)((ij[j] / ND) & 1);
-          pend_s[0] = sc;
+        const uint32_t taddr = tmem + lane_off + (uint32_t)(blk * NPAD);
+#pragma unroll
+        for (int c0 = 0; c0 < NPAD; c0 += 16) {
+          uint32_t v0[8], v1[8];
+          ld8(taddr + c0, v0);
+          ld8(taddr + c0 + 8, v1);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            acc[c0 + i] = fmaf(sc, __uint_as_float(v0[i]), acc[c0 + i]);
+            acc[c0 + 8 + i] = fmaf(sc, __uint_as_float(v1[i]), acc[c0 + 8 + i]);
+          }
+        }
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_de + 8 * blk);
+      }
+      if (ls == SUBS - 1) {   // done with the unit's scale words
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_we + 8 * (ui % kNW));
+      }
+      if (ls == SUBS - 1 && wk.unit_ends_segment(ui)) {
+        // ---- the segment is finished: y directly, or through the split-K
+        // workspace when the tile is shared with other CTAs
+        const int tile = wk.tile;
+        const int row = tile * kRows + r;
+        if (wk.seg_u0 == 0 && seg_u1 == U) {
+#pragma unroll
+          for (int i = 0; i < NPAD; ++i)
+            if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(acc[i]);
         } else {
-          pend_blk[1] = ij[j] % ND;
-          pend_par[1] = (uint32_t)((ij[j] / ND) & 1);
-          pend_s[1] = sc;
-        }
-        ++pend_n;
-      }
-    }
-
-    // ---- end of a segment: finish it and write y (directly, or through the
-    // split-K workspace when the tile is shared with other CTAs)
-    const bool seg_end = ls == SUBS - 1 && (ui + 1 == nunits || uit + 1 == U);
-    if (seg_end) {
+          const int slot = first_seg ? 0 : 1;
+          float* dst = p.scratch + (((size_t)blockIdx.x * 2 + slot) * kRows + r) * NPAD;
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-        if (i < pend_n) drain(pend_blk[i], pend_par[i], pend_s[i]);
-      pend_n = 0;
-      const int row = tile * kRows + r;
-      const bool full = seg_u0 == 0 && seg_u1 == U;
-      if (full) {
-#pragma unroll
-        for (int i = 0; i < HALF; ++i) {
-          const int mm = h * HALF + i;
-          if (mm < p.m && row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(acc[i]);
-        }
-      } else {
-        const int slot = first_seg ? 0 : 1;
-        float* dst = p.scratch + (((size_t)blockIdx.x * 2 + slot) * kRows + r) * NPAD + h * HALF;
-#pragma unroll
-        for (int i = 0; i < HALF; i += 4)
-          __stcg(reinterpret_cast<float4*>(dst + i), make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]));
-        __threadfence();
-        __syncthreads();
-        counted[slot] = true;
-        if (tid == 0) {
-          const long long tu0 = (long long)tile * U, tu1 = tu0 + U - 1;
-          const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu1 + 1) * P - 1) / T);
-          const int old = atomicAdd(p.counters + tile, 1);
-          *last_flag = old == c1 - c0;
-          if (old == c1 - c0) p.counters[tile] = 0;   // left at 0 for the next launch
-        }
-        __syncthreads();
-        if (*last_flag) {
+          for (int i = 0; i < NPAD; i += 4)
+            __stcg(reinterpret_cast<float4*>(dst + i),
+                   make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]));
           __threadfence();
+          asm volatile("bar.sync 1, 128;" ::: "memory");
           const long long tu0 = (long long)tile * U, tu1 = tu0 + U - 1;
           const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu1 + 1) * P - 1) / T);
-          float sum[HALF];
+          if (etid == 0) {
+            const int old = atomicAdd(p.counters + tile, 1);
+            *last_flag = old == c1 - c0;
+            if (old == c1 - c0) p.counters[tile] = 0;   // left at 0 for the next launch
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (*last_flag) {
+            __threadfence();
+            // acc is in the workspace already: it becomes the sum, in CTA order
+            float (&sum)[NPAD] = acc;
 #pragma unroll
-          for (int i = 0; i < HALF; ++i) sum[i] = 0.0f;
-          for (int c = c0; c <= c1; ++c) {
-            const long long bc = (long long)c * T / P;
-            const int cslot = bc >= tu0 ? 0 : 1;     // the tile is CTA c's first, or its last
-            const float* src = p.scratch + (((size_t)c * 2 + cslot) * kRows + r) * NPAD + h * HALF;
+            for (int i = 0; i < NPAD; ++i) sum[i] = 0.0f;
+            for (int c = c0; c <= c1; ++c) {
+              const long long bc = (long long)c * T / P;
+              const int cslot = bc >= tu0 ? 0 : 1;     // the tile is CTA c's first, or its last
+              const float* src = p.scratch + (((size_t)c * 2 + cslot) * kRows + r) * NPAD;
 #pragma unroll
-            for (int i = 0; i < HALF; i += 4) {
-              const float4 f = __ldcg(reinterpret_cast<const float4*>(src + i));
-              sum[i] += f.x;
-              sum[i + 1] += f.y;
-              sum[i + 2] += f.z;
-              sum[i + 3] += f.w;
+              for (int i = 0; i < NPAD; i += 4) {
+                const float4 f = __ldcg(reinterpret_cast<const float4*>(src + i));
+                sum[i] += f.x;
+                sum[i + 1] += f.y;
+                sum[i + 2] += f.z;
+                sum[i + 3] += f.w;
+              }
             }
-          }
 #pragma unroll
-          for (int i = 0; i < HALF; ++i) {
-            const int mm = h * HALF + i;
-            if (mm < p.m && row < p.rows) p.y[(size_t)mm * p.rows + row] = __float2half_rn(sum[i]);
+            for (int i = 0; i < NPAD; ++i)
+              if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(sum[i]);
           }
+          asm volatile("bar.sync 1, 128;" ::: "memory");   // last_flag is read before it is reused
+          first_seg = false;
         }
-      }
-      first_seg = false;
 #pragma unroll
-      for (int i = 0; i < HALF; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < NPAD; ++i) acc[i] = 0.0f;
+      }
     }
   }
 
   // ---- teardown.  After an abort: the copies and MMAs this CTA issued are
   // let land (bounded) before its shared and tensor memory are released --
-  // only the last load issued into each slot and the last two MMA batches can
-  // still be in flight -- and the split-K counters of its partial tiles that
-  // it never reached are brought back to zero, so the next launch counts
-  // right (y of this launch is undefined).
+  // only the last load issued into each slot and the last few sub-stages'
+  // MMAs can still be in flight.  (The epilogue completed the split-K
+  // counters.)
   fence_before();
   __syncthreads();
   if (tid == 0 && *abort_flag) {
@@ -585,25 +671,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
       while (!mbar_try(bar, par))
         if (global_ns() - t0 > lim) break;
     };
+    const int w_issued = pub[0], x_issued = pub[1];
+    const int s_mma = pub[2] > pub[3] ? pub[2] : pub[3];
     for (int ui = max(0, w_issued - kNW); ui < w_issued; ++ui)
-      settle(bar_w + 8 * (ui % kNW), (uint32_t)((ui / kNW) & 1));
+      settle(bar_wf + 8 * (ui % kNW), (uint32_t)((ui / kNW) & 1));
     for (int x = max(0, x_issued - kNX); x < x_issued; ++x)
-      settle(bar_x + 8 * (x % kNX), (uint32_t)((x / kNX) & 1));
-    for (int x = max(0, s_mma - 2); x < s_mma; ++x)
-      settle(bar_a + 8 * (x & 1), (uint32_t)((x >> 1) & 1));
-    const int t_first = (int)(u_begin / U), t_last = (int)((u_end - 1) / U);
-    for (int k = 0; k < 2; ++k) {
-      const int tile = k == 0 ? t_first : t_last;
-      if (k == 1 && t_last == t_first) break;
-      const long long tu0 = (long long)tile * U;
-      const bool partial = k == 0 ? (u_begin > tu0 || u_end < tu0 + U) : (u_end < tu0 + U);
-      if (!partial || counted[k]) continue;
-      const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu0 + U) * P - 1) / T);
-      if (atomicAdd(p.counters + tile, 1) == c1 - c0) p.counters[tile] = 0;
-    }
+      settle(bar_xf + 8 * (x % kNX), (uint32_t)((x / kNX) & 1));
+    for (int x = max(0, s_mma - 4); x < s_mma; ++x)
+      settle(bar_dn + 8 * (x % kRD), (uint32_t)((x / kRD) & 1));
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols)
                  : "memory");
@@ -667,9 +745,10 @@ int tc_sms() {
 int npad_of(int m) { return ((m + 15) / 16) * 16; }
 
 size_t tc_smem(int npad) {
-  // 1024 alignment slack + weight ring + x ring + barriers and flags; at
+  // 1024 alignment slack + weight ring + x ring + barriers and flags (at
+  // most 8 * (2 kNW + kNX + NA + kRD + ND) + 28 bytes); at
   // least 120 KB, so that one CTA (and one tensor-memory allocation) per SM
-  const size_t need = 1024 + (size_t)kNW * kStageW + (size_t)kNX * 2 * npad * 128 + 512;
+  const size_t need = 1024 + (size_t)kNW * kStageW + (size_t)kNX * 2 * npad * 128 + 1024;
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
