@@ -305,6 +305,23 @@ def run_reference(args, rank, world):
 # the GPU arm
 # ---------------------------------------------------------------------------
 
+def run_batch_only(args, local):
+    """--batch-only M: the verification-batch layer set (seven 2:4 g128
+    matrices) at M rows, timed as in batch_m; for ncu captures of the batch
+    kernels."""
+    import torch
+    import sparse_weight_only_gb300 as swo
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    swo.build()
+    swo.load()
+    stream = torch.cuda.Stream(device=dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 126 * 2 ** 20
+    out = run_batch_sweep(args, swo, dev, stream, l2, None, (args.batch_only,))
+    print(json.dumps({"batch_only": args.batch_only, "config4": out}), flush=True)
+    return 0
+
+
 def run_ours(args, rank, world, local):
     import torch
     import sparse_weight_only_gb300 as swo
@@ -434,6 +451,14 @@ def run_ours(args, rank, world, local):
     else:
         per_step = len(gvs)
     launches = per_step * args.steps
+
+    if args.step_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "GB/s",
+                              "ms_per_step": ms_step, "steps": args.steps,
+                              "note": "--step-only: the headline region alone (profiling)"}),
+                  flush=True)
+        return 0
 
     # the survey's protocol as well: a graph of >= 200 back-to-back launches
     # (whole steps, rotating copies), median of 10 timed replays
@@ -901,6 +926,10 @@ def main(argv=None):
                     help="skip the one-GEMV-at-a-time sweep over the single and large layers")
     ap.add_argument("--no-batch", action="store_true",
                     help="skip the small-M (config 4) sweep")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the headline step region alone and stop (profiling)")
+    ap.add_argument("--batch-only", type=int, default=0, metavar="M",
+                    help="run only the verification-batch layer set at M rows (profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -910,6 +939,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, rank, world)
+        if args.batch_only:
+            return run_batch_only(args, local)
         return run_ours(args, rank, world, local)
     finally:
         if world > 1:

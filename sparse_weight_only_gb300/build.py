@@ -58,19 +58,29 @@ def _stamp(files: list[str] | None = None) -> str:
     return h.hexdigest()
 
 
+# Build variants: the product library, and the checked build (a debugging
+# aid: the product kernels validate every decoded code and index).
+VARIANTS = {None: ([], LIB, BUILD),
+            "checked": (["-DSGEMV_CHECKED"], os.path.join(HERE, "libsgemv_checked.so"),
+                        os.path.join(HERE, "_build_checked"))}
+
+
 def build(force: bool = False, verbose: bool = False,
-          extra: list[str] | None = None) -> str:
-    stamp_path = os.path.join(BUILD, "stamp")
-    stamp = _stamp()
-    if (not force and os.path.exists(LIB) and os.path.exists(stamp_path)
+          extra: list[str] | None = None, variant: str | None = None) -> str:
+    vflags, lib, build_dir = VARIANTS[variant]
+    if variant is None:
+        lib, build_dir = LIB, BUILD
+    stamp_path = os.path.join(build_dir, "stamp")
+    stamp = _stamp() + " ".join(vflags + (extra or []))
+    if (not force and os.path.exists(lib) and os.path.exists(stamp_path)
             and open(stamp_path).read() == stamp):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    flags = ARCH + NVCC_FLAGS + (extra or [])
+    flags = ARCH + NVCC_FLAGS + vflags + (extra or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [cc, "-c", src, "-o", obj] + flags
         if verbose:
             cmd += ["-Xptxas", "-v"]
@@ -84,17 +94,18 @@ def build(force: bool = False, verbose: bool = False,
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static",
                                                       "-Xcompiler", "-fPIC"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_path, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                variant="checked" if "--checked" in sys.argv else None))

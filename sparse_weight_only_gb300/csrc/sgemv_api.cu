@@ -90,6 +90,10 @@ int dev_err_to_status(int word) {
       return fail(SGEMV_ERR_TIMEOUT,
                   "a bounded device wait gave up: a batch kernel's copies, MMAs or split-K "
                   "partial sums did not arrive in time; the outputs of that call are undefined");
+    case sgemv::kDevErrChecked:
+      return fail(SGEMV_ERR_ARG,
+                  "checked build: a product kernel decoded a 2:4 position pair that does not "
+                  "ascend, or an index outside its row (the packed weight is corrupt)");
     default:
       return fail(SGEMV_ERR_CUDA, "device error word %d", word);
   }

@@ -84,6 +84,30 @@ constexpr int kDevErrNonfinite = 1;
 constexpr int kDevErrRange = 2;
 constexpr int kDevErrBadIndex = 3;
 constexpr int kDevErrTimeout = 4;
+constexpr int kDevErrChecked = 5;   // checked build: a decoded code or index left its range
+
+// The checked build (-DSGEMV_CHECKED, a debugging aid) makes the product
+// kernels validate what they decode -- every 2:4 position nibble ascends,
+// every group and chunk index stays inside its row -- and record
+// kDevErrChecked instead of reading out of range (never a trap).
+#ifdef SGEMV_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+// Nonzero unless each of the eight 2:4 position nibbles a | b << 2 of w has
+// a < b.
+__device__ __forceinline__ uint32_t bad_codes24(uint32_t w) {
+  uint32_t bad = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t c = (w >> (4 * i)) & 0xFu;
+    bad |= (uint32_t)((c & 3u) >= (c >> 2));
+  }
+  return bad;
+}
+__device__ __forceinline__ void report_checked(int* err) { atomicCAS(err, 0, kDevErrChecked); }
 
 // ---- format kernels (sgemv_format.cu) ----
 // Per-row group sizes of a matrix (rowg NULL: L.group for every row) and

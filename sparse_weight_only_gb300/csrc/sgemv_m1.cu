@@ -312,9 +312,13 @@ struct Producer {
 
   int vstep, sstep_row;   // pointer steps from the end of a row to the next row
   int next_begin;          // first launch row of the next matrix (kMany)
+  const M1Params* p_;      // (checked build) the launch and the current row
+  int row_;
 
   __device__ __forceinline__ void set_row(const M1Params& p, int row, int lane) {
     using C = M1Cfg<N>;
+    p_ = &p;
+    row_ = row;
     seg = seg_from<MODE>(p, seg, row);
     const M1Seg& sg = p.seg[seg];
     const int lr = row - sg.row_begin;
@@ -344,7 +348,17 @@ struct Producer {
   // only this lane reads.  A lane without a chunk in the item copies
   // nothing (its result is discarded).
   __device__ __forceinline__ void issue(uint32_t s16, uint32_t s8) const {
-    const bool on = vleft > 0;
+    bool on = vleft > 0;
+    if constexpr (kChecked) {
+      // the chunk and its scale/zero word(s) lie inside this row
+      const M1Seg& sg = p_->seg[seg];
+      const int64_t ch = vp - (sg.vals + (size_t)(row_ - sg.row_begin) * p_->cstride);
+      const int64_t gw = sp - (sg.sz + (size_t)(row_ - sg.row_begin) * sg.gstride);
+      if (on && (ch < 0 || ch >= p_->cstride || gw < 0 || gw + (g64 ? 1 : 0) >= sg.gstride)) {
+        report_checked(p_->err);
+        on = false;
+      }
+    }
     cp_async_if<16>(on, s16, vp);
     cp_async_if<8>(on, s8 + kIdxOff, ip);
     if (g64)
@@ -362,6 +376,7 @@ struct Producer {
     if (--left > 0) return true;
     if (++j < nrw) {
       const int row = r0 + warp + kNW * j;
+      row_ = row;
       if (row < next_begin) {   // same matrix: step the pointers
         vp += vstep;
         ip += vstep;
@@ -514,7 +529,13 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
         cp_wait<kS - 1>();   // this lane's copies of this item landed
         const bool valid = ci < lane_items;
         const uint4 v = lds128(ring16 + so);
-        const uint2 ix = lds64(ring8 + so + kIdxOff);
+        uint2 ix = lds64(ring8 + so + kIdxOff);
+        if constexpr (kChecked && N == 2) {
+          if (valid && (bad_codes24(ix.x) | bad_codes24(ix.y))) {
+            report_checked(p.err);
+            ix = make_uint2(0x44444444u, 0x44444444u);
+          }
+        }
         const uint2 s2 = lds64(ring8 + so + kSzOff);
         const uint32_t sa = valid ? s2.x : 0u;   // ragged slice: zero contribution
         const uint32_t sb = valid ? s2.y : 0u;

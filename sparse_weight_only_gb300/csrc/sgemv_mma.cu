@@ -395,10 +395,18 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
         v_g8 = lds128(wb + W.vals_off + lr_g8 * W.vst + cc * 16);
         i_g8 = lds64(wb + W.idx_off + lr_g8 * W.ist + cc * 8);
       }
+      if constexpr (kChecked && N == 2) {
+        if ((vg && (bad_codes24(i_g.x) | bad_codes24(i_g.y))) ||
+            (vg8 && (bad_codes24(i_g8.x) | bad_codes24(i_g8.y)))) {
+          report_checked(p.err);
+          if (vg) i_g = make_uint2(0x44444444u, 0x44444444u);
+          if (vg8) i_g8 = make_uint2(0x44444444u, 0x44444444u);
+        }
+      }
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
         if (N == 1 && c * CPC + kt * 32 >= p.cols) break;   // ragged 1:4 tail
-        const int G = (c * CPC + kt * 32) >> p.gshift;
+        int G = (c * CPC + kt * 32) >> p.gshift;
         if (G != cur_group) {
           if (cur_group >= 0) {
 #pragma unroll
@@ -411,6 +419,12 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
             }
           }
           cur_group = G;
+          if constexpr (kChecked) {
+            if (G - g0 < 0 || G - g0 >= W.gs) {
+              report_checked(p.err);
+              G = g0;
+            }
+          }
           const uint32_t w_g = vg ? lds32(wb + W.sz_off + lr_g * W.sst + (G - g0) * 4) : 0x3C00u;
           const uint32_t w_g8 = vg8 ? lds32(wb + W.sz_off + lr_g8 * W.sst + (G - g0) * 4) : 0x3C00u;
           group_consts(w_g, s_g, zc_g);

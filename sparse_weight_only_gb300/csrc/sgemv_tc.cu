@@ -442,16 +442,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     const int quad = warp & 3, h = warp >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    int uit = uit0;
+    int uit = uit0, dtile = tile0;   // dtile: read by the checked build only
     for (int s = 0; s < nsub; ++s) {
       const int ui = s / SUBS, ls = s % SUBS;
-      if (ls == 0 && ui > 0 && ++uit == U) uit = 0;
+      if (ls == 0 && ui > 0 && ++uit == U) {
+        uit = 0;
+        ++dtile;
+      }
       const uint32_t wslot = wring + (uint32_t)((ui % kNW) * kStageW);
       if (ls == 0 && !__all_sync(0xffffffffu, wait(bar_wf + 8 * (ui % kNW), (uint32_t)((ui / kNW) & 1))))
         break;
       const int scol0 = uit * UNIT_COLS + ls * 128;
       const int g0 = ((uit * UNIT_COLS) >> p.gshift) & ~3;
-      const int myG = (scol0 + 64 * h) >> p.gshift;
+      int myG = (scol0 + 64 * h) >> p.gshift;
+      if constexpr (kChecked) {
+        if (myG - g0 < 0 || myG - g0 >= kSzWords) {
+          report_checked(p.err);
+          myG = g0;
+        }
+      }
       const uint32_t szw = lds32(wslot + kSzOff + (uint32_t)(r * 32 + (myG - g0) * 4));
       uint32_t a0[8], a1[8];
       uint32_t m0, m1;
@@ -468,6 +477,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
         }
         m0 = ix.x;
         m1 = ix.y;
+        if constexpr (kChecked) {
+          // valid rows and columns only: the zero padding past the matrix
+          // (rows of the last tile, columns past K) is never multiplied
+          const int colv = uit * UNIT_COLS + ls * 128 + 64 * h;
+          const bool rowv = dtile * kRows + r < p.rows;
+          if (rowv && ((colv < p.cols && bad_codes24(m0)) || (colv + 32 < p.cols && bad_codes24(m1)))) {
+            report_checked(p.err);
+            m0 = m1 = 0x44444444u;
+          }
+        }
       } else {
         const uint2 v = lds64(wslot + kValsOff +
                               (uint32_t)(r * 64 + ((ls ^ ((r >> 1) & 3)) << 4) + h * 8));
