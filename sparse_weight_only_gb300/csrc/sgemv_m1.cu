@@ -593,6 +593,10 @@ __global__ void __launch_bounds__(kNT, 1) k_m1_dual(const __grid_constant__ M1Du
     m1_body<1, kMany>(p.b, blockIdx.x - p.grid_a);
 }
 
+// Time of a 1:4 chunk against a 2:4 chunk in the M=1 kernel (a CTA-time
+// trace of the mixed q/k/v launch; 1.3 gave the shortest step of 1.0-1.5)
+constexpr double kCost14 = 1.3;
+
 int g_num_sms[64] = {0};
 
 int num_sms() {
@@ -741,10 +745,12 @@ cudaError_t launch_m1_group_dual(const Layout* L2, const RunArgs* a2, int n2, co
       return cudaErrorNotSupported;
   const int sms = num_sms();
   if (sms < 2) return cudaErrorNotSupported;
-  // CTAs in proportion to each part's packed chunks (its weight bytes)
+  // CTAs in proportion to each part's time: its chunks (32 kept weights
+  // each) times the measured cost of a chunk, kCost14 for 1:4 (larger pair
+  // tables and units of two quads) against 1 for 2:4
   double b2 = 0.0, b1 = 0.0;
   for (int i = 0; i < n2; ++i) b2 += (double)L2[i].rows * L2[i].chunks;
-  for (int i = 0; i < n1; ++i) b1 += (double)L1[i].rows * L1[i].chunks;
+  for (int i = 0; i < n1; ++i) b1 += kCost14 * L1[i].rows * L1[i].chunks;
   if (b2 <= 0.0 || b1 <= 0.0) return cudaErrorNotSupported;
   int c2 = (int)(sms * b2 / (b1 + b2) + 0.5);
   c2 = c2 < 1 ? 1 : (c2 > sms - 1 ? sms - 1 : c2);
