@@ -651,8 +651,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
 #pragma unroll
             for (int i = 0; i < NPAD; ++i) sum[i] = 0.0f;
             for (int c = c0; c <= c1; ++c) {
+              // the slot CTA c wrote this tile to: its first split segment
+              // goes to slot 0 -- the tile is that when CTA c starts inside
+              // it, or when CTA c starts before it on a tile boundary (its
+              // first tile then was whole, written to y directly)
               const long long bc = (long long)c * T / P;
-              const int cslot = bc >= tu0 ? 0 : 1;     // the tile is CTA c's first, or its last
+              const int cslot = bc >= tu0 || bc % U == 0 ? 0 : 1;
               const float* src = p.scratch + (((size_t)c * 2 + cslot) * kRows + r) * NPAD;
 #pragma unroll
               for (int i = 0; i < NPAD; i += 4) {

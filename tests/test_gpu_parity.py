@@ -147,6 +147,23 @@ def test_run_parity_all_m(native, orc, m):
                 f"m={m} N={n_keep}")
 
 
+@pytest.mark.parametrize("n_keep,m", [(2, 17), (1, 33)])
+def test_run_parity_more_tiles_than_ctas(native, orc, n_keep, m):
+    """The batch kernel's split-K with more 128-row tiles than CTAs: a CTA
+    may cover a whole tile (written to y directly) before a shared one, so
+    its partial of the shared tile sits in its first workspace slot.  At
+    20000 x 1024 five tiles are completed through such a CTA."""
+    rows, cols, group = 20000, 1024, 128
+    W = synth.weight_outliers(rows + n_keep, rows, cols)
+    p = orc.pack(W, n_keep, group)
+    h = native.SparseGemv(rows, cols, n_keep, group, max_m=m)
+    h.import_canonical(p.vals, p.idx, p.scale, p.zero)
+    x = synth.activations(m + 5, m, cols)
+    y = _run(h, x)
+    check_y(orc, y, orc.matvec(p, x), np.abs(orc.dequant(p)).sum(axis=1),
+            f"{rows}x{cols} {n_keep}:4 m={m}")
+
+
 def test_run_host_matches_device(native, orc):
     rows, cols, n_keep, group = 130, 1024, 2, 64
     W = _weight(99, rows, cols, "outliers")
