@@ -256,6 +256,16 @@ struct Walk {
   }
 };
 
+// The workspace slot in which the first CTA sharing a tile (c0, whose range
+// starts at unit b0) wrote it: slot 0 holds a CTA's first split segment,
+// and the tile is c0's first one when c0 starts inside it or on a tile
+// boundary (a whole first tile goes to y directly); otherwise slot 1.
+// Every later CTA sharing the tile starts inside it: slot 0.
+__device__ __forceinline__ int split_slot0(int c0, long long tu0, long long T, int P, int U) {
+  const long long b0 = (long long)c0 * T / P;
+  return b0 >= tu0 || b0 % U == 0 ? 0 : 1;
+}
+
 // The k-steps of one sub-stage: which are inside K, which start and end a
 // group instance, and the instance each belongs to.  An instance never
 // spans two sub-stages (a 256-column group is two instances, each scaled
@@ -320,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + (misc - base) + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(sm + (misc - base) + 8);
   volatile int* pub = reinterpret_cast<volatile int*>(sm + (misc - base) + 12);  // w, x, mma ends
+  // the tile whose split-K sum this CTA does after its teardown barrier, or -1
+  volatile int* final_tile = reinterpret_cast<volatile int*>(sm + (misc - base) + 32);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -342,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     for (int i = 0; i < kRD; ++i) mbar_init(bar_dn + 8 * i, 1);
     for (int i = 0; i < ND; ++i) mbar_init(bar_de + 8 * i, 4);
     *abort_flag = 0;
+    *final_tile = -1;
     pub[0] = pub[1] = pub[2] = pub[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -634,30 +647,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           for (int i = 0; i < NPAD; i += 4)
             __stcg(reinterpret_cast<float4*>(dst + i),
                    make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]));
-          __threadfence();
+          // publish: the named barrier orders every epilogue thread's
+          // partial before the arrival, which releases them at GPU scope
+          // (and, for the arrival that completes the tile, acquires the
+          // other CTAs' partials)
           asm volatile("bar.sync 1, 128;" ::: "memory");
           const long long tu0 = (long long)tile * U, tu1 = tu0 + U - 1;
           const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu1 + 1) * P - 1) / T);
           if (etid == 0) {
-            const int old = atomicAdd(p.counters + tile, 1);
-            *last_flag = old == c1 - c0;
-            if (old == c1 - c0) p.counters[tile] = 0;   // left at 0 for the next launch
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                         : "=r"(old)
+                         : "l"(p.counters + tile)
+                         : "memory");
+            const bool done = old == c1 - c0;
+            if (done) p.counters[tile] = 0;   // left at 0 for the next launch
+            // the CTA's last segment: the whole CTA sums after its teardown
+            // barrier (every role is finished then)
+            const bool defer = done && ui + 1 == nunits;
+            if (defer) *final_tile = tile;
+            *last_flag = done && !defer;
           }
           asm volatile("bar.sync 1, 128;" ::: "memory");
           if (*last_flag) {
-            __threadfence();
-            // acc is in the workspace already: it becomes the sum, in CTA order
+            // a tile completed in mid-run: the epilogue threads sum it, one
+            // row each, in CTA order
+            const int slot0 = split_slot0(c0, tu0, T, P, U);
             float (&sum)[NPAD] = acc;
 #pragma unroll
             for (int i = 0; i < NPAD; ++i) sum[i] = 0.0f;
             for (int c = c0; c <= c1; ++c) {
-              // the slot CTA c wrote this tile to: its first split segment
-              // goes to slot 0 -- the tile is that when CTA c starts inside
-              // it, or when CTA c starts before it on a tile boundary (its
-              // first tile then was whole, written to y directly)
-              const long long bc = (long long)c * T / P;
-              const int cslot = bc >= tu0 || bc % U == 0 ? 0 : 1;
-              const float* src = p.scratch + (((size_t)c * 2 + cslot) * kRows + r) * NPAD;
+              const float* src =
+                  p.scratch + (((size_t)c * 2 + (c == c0 ? slot0 : 0)) * kRows + r) * NPAD;
 #pragma unroll
               for (int i = 0; i < NPAD; i += 4) {
                 const float4 f = __ldcg(reinterpret_cast<const float4*>(src + i));
@@ -687,6 +708,65 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   // counters.)
   fence_before();
   __syncthreads();
+
+  // ---- the split-K sum of the tile this CTA completed last, by every
+  // thread: float4 groups of the partial tiles in row-major order (coalesced
+  // loads), up to 16 partial loads in flight per thread, summed in CTA order
+  // like the epilogue's (so y does not depend on which path summed it)
+  {
+    const int ftile = *final_tile;
+    if (ftile >= 0) {
+      constexpr int G = NPAD / 4;                  // float4 groups per row
+      const long long tu0 = (long long)ftile * U, tu1 = tu0 + U - 1;
+      const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu1 + 1) * P - 1) / T);
+      const int slot0 = split_slot0(c0, tu0, T, P, U);
+      for (int it0 = tid; it0 < kRows * G; it0 += 2 * kThreads) {
+        float4 s2[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) s2[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int cb = c0; cb <= c1; cb += 8) {
+          float4 v[2][8];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int it = it0 + k * kThreads;
+            const int r = it / G, g = it % G;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int c = cb + q;
+              v[k][q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+              if (it < kRows * G && c <= c1)
+                v[k][q] = __ldcg(reinterpret_cast<const float4*>(
+                    p.scratch + (((size_t)c * 2 + (c == c0 ? slot0 : 0)) * kRows + r) * NPAD + 4 * g));
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (cb + q <= c1) {
+                s2[k].x += v[k][q].x;
+                s2[k].y += v[k][q].y;
+                s2[k].z += v[k][q].z;
+                s2[k].w += v[k][q].w;
+              }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int it = it0 + k * kThreads;
+          if (it >= kRows * G) continue;
+          const int r = it / G, g = it % G;
+          const int row = ftile * kRows + r;
+          const float o[4] = {s2[k].x, s2[k].y, s2[k].z, s2[k].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = 4 * g + q;
+            if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(o[q]);
+          }
+        }
+      }
+    }
+  }
+
   if (tid == 0 && *abort_flag) {
     const unsigned long long lim = p.wait_ns;
     auto settle = [&](uint32_t bar, uint32_t par) {
