@@ -208,6 +208,56 @@ def read_traffic(kernel_tag: str):
     return ent
 
 
+TRAFFIC_FILES = ["sgemv_m1.cu", "sgemv_internal.cuh", "sgemv_api.cu"]
+
+
+def record_traffic(csv_path: str, out_path: str, command: str) -> int:
+    """Writes the per-step DRAM record from an ncu CSV log holding the k_m1
+    launches of one grouped step (dram__bytes_read.sum, dram__bytes_write.sum
+    and gpu__time_duration.sum per launch), stamped with the current source of
+    those kernels -- the record is re-taken, never re-stamped."""
+    import csv
+    from sparse_weight_only_gb300.build import _stamp
+    per = {}
+    hdr = None
+    with open(csv_path) as f:
+        for row in csv.reader(f):
+            if not row:
+                continue
+            if row[0] == "ID":
+                hdr = row
+                continue
+            if hdr is None or len(row) != len(hdr):
+                continue
+            d = dict(zip(hdr, row))
+            ent = per.setdefault(int(d["ID"]), {"kernel": d["Kernel Name"]})
+            ent[d["Metric Name"]] = float(d["Metric Value"].replace(",", ""))
+    launches = [per[k] for k in sorted(per)]
+    if not launches or any("dram__bytes_read.sum" not in l for l in launches):
+        print(f"no DRAM counters in {csv_path}", file=sys.stderr)
+        return 1
+    total = sum(l["dram__bytes_read.sum"] + l.get("dram__bytes_write.sum", 0.0) for l in launches)
+    rec = {"sgemv_layerset_m1": {
+        "bytes_per_step": int(total),
+        "algorithmic_bytes_per_step": int(step_bytes(workload(0), 1)),
+        "launches_per_step": len(launches),
+        "per_launch": [{"kernel": l["kernel"].split("(")[0].split("::")[-1],
+                        "dram_bytes": int(l["dram__bytes_read.sum"] + l.get("dram__bytes_write.sum", 0.0)),
+                        "ncu_us": round(l.get("gpu__time_duration.sum", 0.0) / 1e3, 3)}
+                       for l in launches],
+        "source_files": TRAFFIC_FILES,
+        "source_stamp": _stamp(TRAFFIC_FILES),
+        "command": command,
+        "note": "sum of dram__bytes_read.sum + dram__bytes_write.sum over the k_m1 launches "
+                "of one grouped step (q+k+v in one launch, o, gate+up, down)",
+    }}
+    with open(out_path, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    print(json.dumps(rec["sgemv_layerset_m1"]))
+    return 0
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline key)
 # ---------------------------------------------------------------------------
@@ -941,7 +991,14 @@ def main(argv=None):
                     help="time the headline step region alone and stop (profiling)")
     ap.add_argument("--batch-only", type=int, default=0, metavar="M",
                     help="run only the verification-batch layer set at M rows (profiling)")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="write the DRAM record of one step from an ncu CSV log and stop")
+    ap.add_argument("--traffic-out", default=os.path.join(ROOT, "profiles", "traffic.json"))
+    ap.add_argument("--traffic-command", default="",
+                    help="the ncu command that produced the CSV (kept in the record)")
     args = ap.parse_args(argv)
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, args.traffic_out, args.traffic_command)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.repeats < 1:
