@@ -52,6 +52,10 @@ constexpr int kStage = 1024;        // bytes per stage
 constexpr int kIdxOff = 512;        // codes after the 512 B of nibbles
 constexpr int kSzOff = 768;         // scale/zero words after the codes
 constexpr int kSmemLimit = 227 * 1024;
+#ifndef SGEMV_M1_PREFETCH_X
+#define SGEMV_M1_PREFETCH_X 1
+#endif
+constexpr bool kPrefetchX = SGEMV_M1_PREFETCH_X != 0;   // L2 prefetch of x before the wait
 constexpr uint32_t kTabAlign = 2048;
 
 // Pair-table geometry.  A unit's code indexes its entries at a 128-byte
@@ -451,6 +455,16 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
     cp_commit();
   }
 
+  // x of the first K slice into L2 while the previous kernel finishes: its
+  // address is known now, its contents only after the wait (a prefetch
+  // returns no data; a later write of x by the previous kernel lands in L2
+  // all the same), so the staging below reads L2 instead of DRAM.
+  if (kPrefetchX && warp == 0) {
+    const int ncols = min(p.cols, p.slice_chunks * C::CPC);
+    const char* xb = reinterpret_cast<const char*>(p.x);
+    for (int off = 128 * lane; off < 2 * ncols; off += 128 * 32)
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(xb + off));
+  }
   pdl_wait();
   pdl_launch_dependents();
 
