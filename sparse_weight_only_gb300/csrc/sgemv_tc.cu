@@ -612,16 +612,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
         const float sc = __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
         const uint32_t taddr = tmem + lane_off + (uint32_t)(blk * NPAD);
 #pragma unroll
-        for (int c0 = 0; c0 < NPAD; c0 += 16) {
-          uint32_t v0[8], v1[8];
+        for (int c0 = 0; c0 < NPAD; c0 += 8) {
+          uint32_t v0[8];
           ld8(taddr + c0, v0);
-          ld8(taddr + c0 + 8, v1);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            acc[c0 + i] = fmaf(sc, __uint_as_float(v0[i]), acc[c0 + i]);
-            acc[c0 + 8 + i] = fmaf(sc, __uint_as_float(v1[i]), acc[c0 + 8 + i]);
-          }
+          for (int i = 0; i < 8; ++i) acc[c0 + i] = fmaf(sc, __uint_as_float(v0[i]), acc[c0 + i]);
         }
         fence_before();
         __syncwarp();
