@@ -297,6 +297,10 @@ constexpr int kEpiWarp0 = 8;           // epilogue warps 8..11 (lane quadrant w 
 constexpr int kMmaWarp = 12;           // MMA issue: warps 12 and 13, alternate sub-stages
 constexpr int kProdWarp = 14;
 constexpr int kRD = 32;                // "sub-stage done" barriers (ring)
+#ifndef SGEMV_TC_ALIGN_PCT
+#define SGEMV_TC_ALIGN_PCT 84
+#endif
+constexpr int kAlignPct = SGEMV_TC_ALIGN_PCT;   // least share of the CTAs a tile-aligned grid keeps
 
 template <int N, int NPAD>
 __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcParams p) {
@@ -880,6 +884,21 @@ cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, c
   p.total_units = (long long)p.ntiles * p.units_per_tile;
   const int cap = sms < max_ctas ? sms : max_ctas;
   p.grid = (int)(p.total_units < cap ? p.total_units : cap);
+  // A grid whose equal unit runs fall on tile boundaries -- k units per CTA
+  // with k dividing the tile's units (each tile shared by exactly U / k CTAs,
+  // no CTA straddling two) or a multiple of them (no split at all) -- when
+  // one exists with at least kAlignPct% of the CTAs: fewer partial tiles and
+  // no split-K publication in mid-run, for a few idle SMs.
+  if (kAlignPct > 0 && p.total_units > p.grid && p.total_units % p.grid != 0) {
+    for (int g = p.grid - 1; 100 * g >= kAlignPct * p.grid; --g) {
+      if (p.total_units % g) continue;
+      const long long k = p.total_units / g;
+      if (p.units_per_tile % k == 0 || k % p.units_per_tile == 0) {
+        p.grid = g;
+        break;
+      }
+    }
+  }
   p.withhold = a.withhold;
   p.wait_ns = a.withhold ? kInjectWaitNs : kWaitLimitNs;
   const size_t smem = tc_smem(NPAD);
