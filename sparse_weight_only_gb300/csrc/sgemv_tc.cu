@@ -71,6 +71,8 @@ struct TcParams {
   int ntiles, units_per_tile;
   long long total_units;
   int grid;
+  int parts;             // >= 2: each tile's units split over a cluster of `parts` CTAs
+                         // (split-K through distributed shared memory); else stream-K
   int withhold;          // failure-detection test hook: no x loads are issued
   unsigned long long wait_ns;
 };
@@ -123,6 +125,26 @@ __device__ __forceinline__ void fence_before() {
 }
 __device__ __forceinline__ void fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Thread-block cluster: a full barrier (release / acquire), the address of
+// the same shared-memory offset in another CTA of the cluster, and a 16-byte
+// load from there.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 // 128-byte-swizzled K-major shared-memory operand (8-row atoms, 1024 B apart)
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
@@ -301,6 +323,10 @@ constexpr int kRD = 32;                // "sub-stage done" barriers (ring)
 #define SGEMV_TC_ALIGN_PCT 50
 #endif
 constexpr int kAlignPct = SGEMV_TC_ALIGN_PCT;   // least share of the SMs a tile-aligned grid keeps
+#ifndef SGEMV_TC_CLUSTER
+#define SGEMV_TC_CLUSTER 1
+#endif
+constexpr bool kClusterMode = SGEMV_TC_CLUSTER != 0;
 
 template <int N, int NPAD>
 __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcParams p) {
@@ -342,8 +368,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
   const int U = p.units_per_tile;
   const long long T = p.total_units;
   const int P = p.grid;
-  const long long u_begin = (long long)blockIdx.x * T / P;
-  const long long u_end = (long long)(blockIdx.x + 1) * T / P;
+  // the CTA's run of (row tile, K unit) units: equal runs of the whole
+  // sequence (stream-K), or -- in cluster mode -- part (rank) q of tile t
+  long long u_begin, u_end;
+  if (p.parts >= 2) {
+    const int t = (int)blockIdx.x / p.parts, q = (int)blockIdx.x % p.parts;
+    u_begin = (long long)t * U + (long long)q * U / p.parts;
+    u_end = (long long)t * U + (long long)(q + 1) * U / p.parts;
+  } else {
+    u_begin = (long long)blockIdx.x * T / P;
+    u_end = (long long)(blockIdx.x + 1) * T / P;
+  }
   const int nunits = (int)(u_end - u_begin);
   const int nsub = nunits * SUBS;
   const int tile0 = (int)(u_begin / U), uit0 = (int)(u_begin % U);
@@ -640,6 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
 #pragma unroll
           for (int i = 0; i < NPAD; ++i)
             if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(acc[i]);
+        } else if (p.parts >= 2) {
+          // cluster mode: the partial tile goes to this CTA's own shared
+          // memory (the weight ring, free once every epilogue thread has read
+          // its last scale word), summed across the cluster after teardown
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          float* stage = reinterpret_cast<float*>(sm) + (size_t)r * NPAD;
+#pragma unroll
+          for (int i = 0; i < NPAD; i += 4)
+            *reinterpret_cast<float4*>(stage + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
         } else {
           const int slot = first_seg ? 0 : 1;
           float* dst = p.scratch + (((size_t)blockIdx.x * 2 + slot) * kRows + r) * NPAD;
@@ -784,6 +828,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
       settle(bar_dn + 8 * (x % kRD), (uint32_t)((x / kRD) & 1));
   }
   __syncthreads();
+
+  // ---- cluster mode: rank q sums rows [q R, (q + 1) R) of the tile, R = 128 /
+  // parts, over every rank's staged partial in rank order (the CTA order of
+  // the stream-K sum, so y is the same bitwise), reading the other ranks'
+  // shared memory directly; a second cluster barrier keeps every CTA's
+  // staged tile alive until all ranks have read it.
+  if (p.parts >= 2) {
+    cluster_sync();
+    constexpr int G = NPAD / 4;                   // float4 groups per row
+    const int q = (int)(blockIdx.x % p.parts), R = kRows / p.parts;
+    const int tile = (int)blockIdx.x / p.parts;
+    for (int it = tid; it < R * G; it += kThreads) {
+      const int rl = it / G, g = it % G, r = q * R + rl;
+      const uint32_t off = base + (uint32_t)((r * G + g) * 16);
+      float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int k0 = 0; k0 < p.parts; k0 += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          v[k] = k0 + k < p.parts ? ld_cluster_f4(mapa_rank(off, (uint32_t)(k0 + k)))
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (k0 + k < p.parts) {
+            sum.x += v[k].x;
+            sum.y += v[k].y;
+            sum.z += v[k].z;
+            sum.w += v[k].w;
+          }
+      }
+      const int row = tile * kRows + r;
+      const float o[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = 4 * g + k;
+        if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(o[k]);
+      }
+    }
+    cluster_sync();
+  }
   if (warp == kMmaWarp) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols)
@@ -883,6 +967,17 @@ cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, c
   p.units_per_tile = (L.cols + UNIT_COLS - 1) / UNIT_COLS;
   p.total_units = (long long)p.ntiles * p.units_per_tile;
   const int cap = sms < max_ctas ? sms : max_ctas;
+  // cluster mode when every tile fits 2..8 CTAs (a power of two, at least
+  // one unit each) within the SMs: no workspace, no counters, no CTA waiting
+  // on a global arrival
+  p.parts = 0;
+  if (kClusterMode && p.ntiles <= cap) {
+    int parts = cap / p.ntiles;
+    parts = parts > 8 ? 8 : parts;
+    parts = parts > p.units_per_tile ? p.units_per_tile : parts;
+    while (parts & (parts - 1)) parts &= parts - 1;
+    if (parts >= 2) p.parts = parts;
+  }
   p.grid = (int)(p.total_units < cap ? p.total_units : cap);
   // A grid whose equal unit runs fall on tile boundaries -- k units per CTA
   // with k dividing the tile's units (each tile shared by exactly U / k CTAs,
@@ -891,7 +986,8 @@ cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, c
   // no split-K publication in mid-run, for some idle SMs.  (Measured on the
   // config-4 layer set: the 11008-row layers run faster on 86 CTAs of one
   // whole tile each than on 152 sharing tiles, by 7% of the step at M = 64.)
-  if (kAlignPct > 0 && p.total_units > p.grid && p.total_units % p.grid != 0) {
+  if (p.parts >= 2) p.grid = p.ntiles * p.parts;
+  if (p.parts < 2 && kAlignPct > 0 && p.total_units > p.grid && p.total_units % p.grid != 0) {
     for (int g = p.grid - 1; 100 * g >= kAlignPct * p.grid; --g) {
       if (p.total_units % g) continue;
       const long long k = p.total_units / g;
@@ -918,11 +1014,15 @@ cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, c
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = p.parts >= 2 ? p.parts : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.parts >= 2 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_tc<N, NPAD>, p);
 }
 
