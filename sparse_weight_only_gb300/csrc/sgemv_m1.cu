@@ -8,11 +8,14 @@
 // kept weight), so the kernel keeps many bytes in flight and issues few
 // instructions per weight:
 //
-//  * Weights stream through a per-warp ring of shared-memory stages filled
-//    by asynchronous copies (cp.async): each lane copies its 16 bytes of
-//    nibbles, 8 bytes of codes and its scale/zero word for the item two
-//    chunks ahead into a region only it reads, so no registers hold data in
-//    flight and no cross-lane synchronisation is needed.  The first stages
+//  * Weights stream through a per-warp ring of two shared-memory stages
+//    filled by asynchronous copies (cp.async): each lane copies its 16 bytes
+//    of nibbles, 8 bytes of codes and its scale/zero word for the item two
+//    ahead into a region only it reads, so no registers hold data in flight
+//    and no cross-lane synchronisation is needed.  A row of a K slice is a
+//    fixed number of items (1 to 4, a template parameter), so copy offsets
+//    and table offsets are constants of the unrolled row, and so are the
+//    ring stages when the row is a whole number of rings.  The first stages
 //    are issued before the programmatic-dependent-launch wait, overlapping
 //    the previous kernel.  (Per-warp bulk TMA copies of the same stages were
 //    measured slower: the items are 128-512 B, too small for the TMA unit.)
@@ -39,15 +42,25 @@
 namespace sgemv {
 namespace {
 
-#ifndef SGEMV_M1_S
-#define SGEMV_M1_S 2
-#endif
 #ifndef SGEMV_M1_NT
 #define SGEMV_M1_NT 512
 #endif
 constexpr int kNT = SGEMV_M1_NT;    // threads per CTA (one CTA per SM)
 constexpr int kNW = kNT / 32;
-constexpr int kS = SGEMV_M1_S;      // ring stages per warp (2 measured best)
+#ifndef SGEMV_M1_D
+#define SGEMV_M1_D 2
+#endif
+#ifndef SGEMV_M1_STATIC
+#define SGEMV_M1_STATIC 2
+#endif
+// Ring stages as constants: 2 = where a row is a whole number of rings
+// (measured best: the smaller loop body of the grouped launches wins); 1 =
+// also by unrolling rows; 0 = never.
+constexpr int kStaticStages = SGEMV_M1_STATIC;
+// Items in flight per warp: item t of a warp's stream sits in ring stage
+// t % kS, and consuming it issues item t + kS.
+constexpr int kS = SGEMV_M1_D;
+static_assert(kS == 2 || kS == 4 || kS == 8, "ring stages: a power of two");
 constexpr int kStage = 1024;        // bytes per stage
 constexpr int kIdxOff = 512;        // codes after the 512 B of nibbles
 constexpr int kSzOff = 768;         // scale/zero words after the codes
@@ -117,28 +130,31 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;");
 }
 
-template <int BYTES>
-__device__ __forceinline__ void cp_async(uint32_t dst, const void* src) {
-  if (BYTES == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(BYTES)
-                 : "memory");
-}
-// The same copy, issued only where `on` is set (a predicated instruction,
-// so lanes without a chunk need no divergent branch).
-template <int BYTES>
-__device__ __forceinline__ void cp_async_if(bool on, uint32_t dst, const void* src) {
-  if (BYTES == 16)
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %2, 0; @p cp.async.cg.shared.global [%0], [%1], 16; }" ::"r"(dst),
-        "l"(src), "r"((int)on)
-        : "memory");
-  else
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %2, 0; @p cp.async.ca.shared.global [%0], [%1], %3; }" ::"r"(dst),
-        "l"(src), "r"((int)on), "n"(BYTES)
-        : "memory");
+// dst + DOFF <- src + SOFF (bytes), issued only where `on` is set when PRED
+// (a predicated instruction, so lanes without a chunk need no branch).
+template <int BYTES, int DOFF, int SOFF, bool PRED>
+__device__ __forceinline__ void cp_async_at(bool on, uint32_t dst, const void* src) {
+  if constexpr (PRED) {
+    if constexpr (BYTES == 16)
+      asm volatile(
+          "{ .reg .pred p; setp.ne.b32 p, %2, 0; @p cp.async.cg.shared.global [%0+%3], [%1+%4], 16; }" ::"r"(dst),
+          "l"(src), "r"((int)on), "n"(DOFF), "n"(SOFF)
+          : "memory");
+    else
+      asm volatile(
+          "{ .reg .pred p; setp.ne.b32 p, %2, 0; @p cp.async.ca.shared.global [%0+%3], [%1+%4], %5; }" ::"r"(dst),
+          "l"(src), "r"((int)on), "n"(DOFF), "n"(SOFF), "n"(BYTES)
+          : "memory");
+  } else {
+    if constexpr (BYTES == 16)
+      asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;" ::"r"(dst), "l"(src), "n"(DOFF),
+                   "n"(SOFF)
+                   : "memory");
+    else
+      asm volatile("cp.async.ca.shared.global [%0+%2], [%1+%3], %4;" ::"r"(dst), "l"(src), "n"(DOFF),
+                   "n"(SOFF), "n"(BYTES)
+                   : "memory");
+  }
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -146,16 +162,18 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
+template <int OFF>
+__device__ __forceinline__ uint4 lds128_at(uint32_t a) {
   uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+%5];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
+               : "r"(a), "n"(OFF));
   return v;
 }
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
+template <int OFF>
+__device__ __forceinline__ uint2 lds64_at(uint32_t a) {
   uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF));
   return v;
 }
 
@@ -252,11 +270,12 @@ __device__ __forceinline__ float sz_zero(uint32_t w) {
 // group scale applied by explicit FMAs so that a row rounds the same way in
 // every launch mode.  G2: the chunk spans two (scale, zero) groups (1:4 with
 // 64-column groups), units 0..7 in the first and 8..15 in the second.
-template <int N, bool G2>
+// TOFF: byte offset of the chunk's table slot from `base`.
+template <int N, bool G2, int TOFF>
 __device__ __forceinline__ float chunk_dot(const uint4& v, const uint2& ix,
                                            uint32_t sa, uint32_t sb, uint32_t base,
                                            uint32_t magic, float acc) {
-  constexpr int E = M1Cfg<N>::E, O = M1Cfg<N>::OFF0;
+  constexpr int E = M1Cfg<N>::E, O = M1Cfg<N>::OFF0 + TOFF;
   float2 a0, a1, a2, a3;
   if (!G2) {
     const ZConst k = zconst(sz_zero(sa));
@@ -297,32 +316,26 @@ __device__ __forceinline__ int seg_from(const M1Params& p, int seg, int row) {
   return MODE == kMany ? seg : 0;
 }
 
-// The copy side of a warp's ring: walks the warp's items (K slices in
-// order; in a slice the warp's rows in order; in a row `ipr` items of 32
-// chunks, item i holding chunk c0 + 32 i + lane of each lane) with
-// per-lane pointers that advance by one item per step.
+// The copy side of a warp's weight stream over one K slice.  It stands at
+// row P of the warp (ordinal `pr`, launch row `row`) with per-lane pointers
+// to the lane's chunk c0 + lane of each stream; item k of the row holds the
+// chunks 32 k further on.
 template <int N, int MODE>
-struct Producer {
-  int sl, j;           // K slice, row ordinal of the warp
-  int left;            // items left in the current row
-  int vleft;           // of them, items in which this lane holds a chunk
-  int seg;             // matrix of the current row
-  int sstep;           // scale/zero words between a lane's consecutive items
-  bool g64;            // two scale/zero words per chunk
-  const uint4* vp;     // this lane's next chunk: nibbles, codes, scale/zero
+struct RowProducer {
+  const uint4* vp;     // nibbles, codes and scale/zero of item 0 of row P
   const uint2* ip;
   const uint32_t* sp;
-  int c0, ipr, lane_items;
+  int sstep;           // scale/zero words between a lane's chunks in consecutive items
+  int sstep_row;       // scale/zero words from row P to row P + kNW (same matrix)
+  int vstep;           // chunks from row P to row P + kNW
+  int next_begin;      // first launch row of the next matrix (kMany)
+  int seg, pr, row;
+  bool g64;            // two scale/zero words per chunk
+  const M1Params* p_;  // (checked build)
 
-  int vstep, sstep_row;   // pointer steps from the end of a row to the next row
-  int next_begin;          // first launch row of the next matrix (kMany)
-  const M1Params* p_;      // (checked build) the launch and the current row
-  int row_;
-
-  __device__ __forceinline__ void set_row(const M1Params& p, int row, int lane) {
+  __device__ __forceinline__ void set_row(const M1Params& p, int c0, int lane) {
     using C = M1Cfg<N>;
     p_ = &p;
-    row_ = row;
     seg = seg_from<MODE>(p, seg, row);
     const M1Seg& sg = p.seg[seg];
     const int lr = row - sg.row_begin;
@@ -332,71 +345,215 @@ struct Producer {
     sp = sg.sz + (size_t)lr * sg.gstride + ((ch * C::CPC) >> sg.gshift);
     sstep = (32 * C::CPC) >> sg.gshift;
     g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
-    vstep = kNW * p.cstride - 32 * ipr;
-    sstep_row = kNW * sg.gstride - sstep * ipr;
+    vstep = kNW * p.cstride;
+    sstep_row = kNW * sg.gstride;
     next_begin = MODE == kMany && seg + 1 < p.nseg ? p.seg[seg + 1].row_begin : 0x7fffffff;
-    left = ipr;
-    vleft = lane_items;
   }
-  __device__ __forceinline__ void start_slice(const M1Params& p, int r0, int warp, int lane) {
-    c0 = sl * p.slice_chunks;
-    const int nch = min(p.slice_chunks, p.chunks - c0);
-    ipr = (nch + 31) >> 5;
-    lane_items = nch > lane ? (nch - lane + 31) >> 5 : 0;
-    j = 0;
+  __device__ __forceinline__ void start(const M1Params& p, int r0, int warp, int c0, int lane) {
+    pr = 0;
+    row = r0 + warp;
     seg = 0;
-    set_row(p, r0 + warp, lane);
+    set_row(p, c0, lane);
   }
-  // Copies this lane's part of the next item into `stage`: 16 bytes of
-  // nibbles, 8 bytes of codes and the scale/zero word(s), each into a region
-  // only this lane reads.  A lane without a chunk in the item copies
-  // nothing (its result is discarded).
-  __device__ __forceinline__ void issue(uint32_t s16, uint32_t s8) const {
-    bool on = vleft > 0;
+  // to the warp's next row (pointers only while it has one)
+  __device__ __forceinline__ void advance(const M1Params& p, int c0, int lane, int nrw) {
+    ++pr;
+    row += kNW;
+    if (pr >= nrw) return;
+    if (row < next_begin) {
+      vp += vstep;
+      ip += vstep;
+      sp += sstep_row;
+    } else {
+      set_row(p, c0, lane);
+    }
+  }
+  // Copies this lane's part of item K of row P into the ring stage at
+  // s16 + SO (nibbles) and s8 + SO (codes, scale/zero): 16 bytes of nibbles,
+  // 8 bytes of codes and the scale/zero word(s), each into a region only
+  // this lane reads.  PRED: only where `on` (the last item of a ragged
+  // slice).
+  template <int K, bool PRED, int SO>
+  __device__ __forceinline__ void issue(uint32_t s16, uint32_t s8, bool on) const {
+    const uint32_t* s = sp + K * sstep;
+    if (!check(vp + 32 * K, s, !PRED || on)) return;
+    cp_async_at<16, SO, K * 512, PRED>(on, s16, vp);
+    cp_async_at<8, SO + kIdxOff, K * 256, PRED>(on, s8, ip);
+    if (g64)
+      cp_async_at<8, SO + kSzOff, 0, PRED>(on, s8, s);
+    else
+      cp_async_at<4, SO + kSzOff, 0, PRED>(on, s8, s);
+  }
+  // The same with K and the stage at run time (the prologue).
+  __device__ __forceinline__ void issue_rt(int k, uint32_t s16, uint32_t s8, bool on) const {
+    const uint32_t* s = sp + k * sstep;
+    if (!check(vp + 32 * k, s, on)) return;
+    cp_async_at<16, 0, 0, true>(on, s16, vp + 32 * k);
+    cp_async_at<8, kIdxOff, 0, true>(on, s8, ip + 32 * k);
+    if (g64)
+      cp_async_at<8, kSzOff, 0, true>(on, s8, s);
+    else
+      cp_async_at<4, kSzOff, 0, true>(on, s8, s);
+  }
+  // (checked build) the chunk at v and its scale/zero word(s) at s lie
+  // inside row P; false after recording an error
+  __device__ __forceinline__ bool check(const uint4* v, const uint32_t* s, bool on) const {
     if constexpr (kChecked) {
-      // the chunk and its scale/zero word(s) lie inside this row
       const M1Seg& sg = p_->seg[seg];
-      const int64_t ch = vp - (sg.vals + (size_t)(row_ - sg.row_begin) * p_->cstride);
-      const int64_t gw = sp - (sg.sz + (size_t)(row_ - sg.row_begin) * sg.gstride);
+      const int64_t ch = v - (sg.vals + (size_t)(row - sg.row_begin) * p_->cstride);
+      const int64_t gw = s - (sg.sz + (size_t)(row - sg.row_begin) * sg.gstride);
       if (on && (ch < 0 || ch >= p_->cstride || gw < 0 || gw + (g64 ? 1 : 0) >= sg.gstride)) {
         report_checked(p_->err);
-        on = false;
+        return false;
       }
     }
-    cp_async_if<16>(on, s16, vp);
-    cp_async_if<8>(on, s8 + kIdxOff, ip);
-    if (g64)
-      cp_async_if<8>(on, s8 + kSzOff, sp);
-    else
-      cp_async_if<4>(on, s8 + kSzOff, sp);
-  }
-  // false once past the warp's last item
-  __device__ __forceinline__ bool advance(const M1Params& p, int r0, int warp, int nrw,
-                                          int lane) {
-    vp += 32;
-    ip += 32;
-    sp += sstep;
-    --vleft;
-    if (--left > 0) return true;
-    if (++j < nrw) {
-      const int row = r0 + warp + kNW * j;
-      row_ = row;
-      if (row < next_begin) {   // same matrix: step the pointers
-        vp += vstep;
-        ip += vstep;
-        sp += sstep_row;
-        left = ipr;
-        vleft = lane_items;
-      } else {
-        set_row(p, row, lane);
-      }
-      return true;
-    }
-    if (++sl >= p.nslices) return false;
-    start_slice(p, r0, warp, lane);
     return true;
   }
 };
+
+// What one warp's item loop over a K slice needs.
+template <int N, int MODE>
+struct SliceCtx {
+  RowProducer<N, MODE>* prod;
+  const M1Params* p;
+  uint32_t ring16, ring8;   // this lane's regions of ring stage 0
+  uint32_t lane_base;       // this lane's table column, chunk slot 0
+  uint32_t magic;
+  uint32_t par;             // (stages at run time) ring offset of the row's first item
+  int c0, nrw, lane;
+  bool last_on;             // this lane holds a chunk in the row's last item
+};
+
+// Item I of the current row (IPR items per row): waits for its copies,
+// reads its ring stage, refills that stage with the item kS ahead in the
+// warp's stream and adds the chunk's contribution to acc.  SO0: the stage
+// of the row's item 0 when it is known at compile time, else -1 (c.par).
+template <int N, int MODE, int IPR, int SO0, int I>
+__device__ __forceinline__ void row_items(SliceCtx<N, MODE>& c, bool g64, float& acc) {
+  if constexpr (I < IPR) {
+    using C = M1Cfg<N>;
+    constexpr bool kRt = SO0 < 0;
+    constexpr int SO = kRt ? 0 : ((SO0 + I) % kS) * kStage;
+    uint32_t r16 = c.ring16, r8 = c.ring8;
+    if constexpr (kRt) {
+      const uint32_t so = (c.par + I * kStage) & (kS * kStage - 1);
+      r16 += so;
+      r8 += so;
+    }
+    constexpr bool kLast = I == IPR - 1;
+    const bool valid = !kLast || c.last_on;
+    cp_wait<kS - 1>();   // this lane's copies of this item landed
+    const uint4 v = lds128_at<SO>(r16);
+    uint2 ix = lds64_at<SO + kIdxOff>(r8);
+    if constexpr (kChecked && N == 2) {
+      if (valid && (bad_codes24(ix.x) | bad_codes24(ix.y))) {
+        report_checked(c.p->err);
+        ix = make_uint2(0x44444444u, 0x44444444u);
+      }
+    }
+    const uint2 s2 = lds64_at<SO + kSzOff>(r8);
+    const uint32_t sa = valid ? s2.x : 0u;   // ragged slice: zero contribution
+    const uint32_t sb = valid ? s2.y : 0u;
+    // refill this stage with the item kS ahead: item K of a later row
+    RowProducer<N, MODE>& q = *c.prod;
+    constexpr int K = (I + kS) % IPR;
+    if constexpr (K == 0) q.advance(*c.p, c.c0, c.lane, c.nrw);
+    if (q.pr < c.nrw) q.template issue<K, K == IPR - 1, SO>(r16, r8, c.last_on);
+    cp_commit();
+    constexpr int TOFF = I * C::SLOTS * 128;
+    if constexpr (N == 1 && MODE == kMany) {
+      if (g64)
+        acc = chunk_dot<N, true, TOFF>(v, ix, sa, sb, c.lane_base, c.magic, acc);
+      else
+        acc = chunk_dot<N, false, TOFF>(v, ix, sa, sb, c.lane_base, c.magic, acc);
+    } else {
+      acc = chunk_dot<N, N == 1 && MODE == kOneG64, TOFF>(v, ix, sa, sb, c.lane_base, c.magic,
+                                                          acc);
+    }
+    row_items<N, MODE, IPR, SO0, I + 1>(c, g64, acc);
+  }
+}
+
+// The first kS items of a slice's stream into the ring, one commit group
+// each (empty past the warp's rows).  The producer is left on the row of
+// the last item issued.
+template <int N, int MODE>
+__device__ __forceinline__ void stream_prologue(RowProducer<N, MODE>& prod, const M1Params& p,
+                                                int r0, int warp, int lane, int c0, int ipr,
+                                                int nrw, bool last_on, uint32_t ring16,
+                                                uint32_t ring8) {
+  if (nrw > 0) prod.start(p, r0, warp, c0, lane);
+  int k = 0;
+#pragma unroll
+  for (int t = 0; t < kS; ++t) {
+    if (t > 0 && k == 0) prod.advance(p, c0, lane, nrw);
+    if (nrw > 0 && prod.pr < nrw)
+      prod.issue_rt(k, ring16 + t * kStage, ring8 + t * kStage, k < ipr - 1 || last_on);
+    cp_commit();
+    k = k + 1 == ipr ? 0 : k + 1;
+  }
+}
+
+// One row of the warp (ordinal j): its IPR items, the warp reduction and
+// the store.
+template <int N, int MODE, int IPR, int SO0>
+__device__ __forceinline__ void one_row(SliceCtx<N, MODE>& c, int r0, int warp, int j, int sl,
+                                        float* part, int& seg) {
+  const M1Params& p = *c.p;
+  const int lr = warp + kNW * j;
+  const int row = r0 + lr;
+  seg = seg_from<MODE>(p, seg, row);
+  const M1Seg& sg = p.seg[seg];
+  const bool g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
+  float acc = 0.0f;
+  row_items<N, MODE, IPR, SO0, 0>(c, g64, acc);
+  if constexpr (SO0 < 0) c.par = (c.par + IPR * kStage) & (kS * kStage - 1);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (c.lane == 0) {
+    __half* yrow = sg.y + (row - sg.row_begin);
+    if (p.nslices == 1) {
+      *yrow = __float2half_rn(acc);
+    } else {
+      const float t = (sl ? part[lr] : 0.0f) + acc;
+      if (sl == p.nslices - 1)
+        *yrow = __float2half_rn(t);
+      else
+        part[lr] = t;
+    }
+  }
+}
+
+// Rows j .. j + RU - 1 of the warp (those it has), unrolled so that the
+// ring stage of every item is a constant.
+template <int N, int MODE, int IPR, int RU, int JJ>
+__device__ __forceinline__ void row_group(SliceCtx<N, MODE>& c, int r0, int warp, int j, int sl,
+                                          float* part, int& seg) {
+  if constexpr (JJ < RU) {
+    if (JJ == 0 || j + JJ < c.nrw) {
+      constexpr bool kStatic = kStaticStages == 1 ? (IPR % kS == 0 || kS % IPR == 0)
+                                               : kStaticStages == 2 && IPR % kS == 0;
+      one_row<N, MODE, IPR, kStatic ? (JJ * IPR) % kS : -1>(c, r0, warp, j + JJ, sl, part, seg);
+      row_group<N, MODE, IPR, RU, JJ + 1>(c, r0, warp, j, sl, part, seg);
+    }
+  }
+}
+
+// The warp's rows of one K slice, IPR items each.
+template <int N, int MODE, int IPR>
+__device__ __forceinline__ void stream_slice(SliceCtx<N, MODE>& c, int r0, int warp, int sl,
+                                             float* part) {
+  constexpr bool kStatic = kStaticStages == 1 ? (IPR % kS == 0 || kS % IPR == 0)
+                                               : kStaticStages == 2 && IPR % kS == 0;
+  constexpr int RU = kStatic && IPR < kS ? kS / IPR : 1;
+  int seg = 0;
+  for (int j = 0; j < c.nrw; j += RU) row_group<N, MODE, IPR, RU, 0>(c, r0, warp, j, sl, part, seg);
+}
+
+// Items per row the kernel is compiled for: 2:4 slices of up to 128
+// chunks, 1:4 of up to 64 (the pair tables of larger slices do not fit).
+template <int N>
+constexpr int max_ipr() { return N == 2 ? 4 : 2; }
 
 // The body of one CTA; `cta` is its index within the launch part that
 // covers these matrices (a launch may hold two parts, one per N).
@@ -421,7 +578,6 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
   const uint32_t ring_s = smem_s + (uint32_t)(tab_bytes + xs_bytes + part_bytes);
   const uint32_t my_ring = ring_s + (uint32_t)(warp * kS * kStage);
   const uint32_t lane_base = smem_s + (uint32_t)((lane >> 4) * S) * 128u + (lane & 15) * 8u;
-  constexpr uint32_t kChunkSlotBytes = C::SLOTS * 128;   // a multiple of 2 KB
   uint32_t magic = 0x4B000000u;  // exponent of 2^23, kept in a register
   asm volatile("" : "+r"(magic));
 
@@ -429,8 +585,6 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
   const int nr = max(0, min(p.rows, r0 + p.rows_per_cta) - r0);
   const int nrw = warp_nrows(warp, nr);
 
-  // ---- the first kS items into the ring (weights only: no dependence on
-  // the previous kernel); one commit group per item, empty past the end
   // The ring starts zeroed: a lane past a ragged slice reads a stage it did
   // not fill, and must find codes in range there (its table slots are zero).
   // (2:4: position nibbles 4 = (0, 1), the smallest code the table holds)
@@ -441,18 +595,24 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
   __syncwarp();
   // this lane's regions of ring stage 0 (nibbles; codes and scale/zero)
   const uint32_t ring16 = my_ring + 16 * lane, ring8 = my_ring + 8 * lane;
-  Producer<N, MODE> prod;
-  bool more = nrw > 0;
-  if (more) {
-    prod.sl = 0;
-    prod.start_slice(p, r0, warp, lane);
-  }
-  for (int st = 0; st < kS; ++st) {
-    if (more) {
-      prod.issue(ring16 + st * kStage, ring8 + st * kStage);
-      more = prod.advance(p, r0, warp, nrw, lane);
-    }
-    cp_commit();
+  RowProducer<N, MODE> prod;
+  SliceCtx<N, MODE> c;
+  c.prod = &prod;
+  c.p = &p;
+  c.ring16 = ring16;
+  c.ring8 = ring8;
+  c.lane_base = lane_base;
+  c.magic = magic;
+  c.nrw = nrw;
+  c.lane = lane;
+
+  // ---- the first two items of slice 0 into the ring (weights only: no
+  // dependence on the previous kernel)
+  {
+    const int nch = min(p.slice_chunks, p.chunks);
+    const int ipr = (nch + 31) >> 5;
+    stream_prologue<N, MODE>(prod, p, r0, warp, lane, 0, ipr, nrw, lane < nch - 32 * (ipr - 1),
+                             ring16, ring8);
   }
 
   // x of the first K slice into L2 while the previous kernel finishes: its
@@ -468,12 +628,13 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
   pdl_wait();
   pdl_launch_dependents();
 
-  int st = 0;   // ring stage of the next item to compute
   for (int sl = 0; sl < p.nslices; ++sl) {
     const int c0 = sl * p.slice_chunks;
     const int nch = min(p.slice_chunks, p.chunks - c0);
     const int ipr = (nch + 31) >> 5;                 // items per row
-    const int lane_items = nch > lane ? (nch - lane + 31) >> 5 : 0;
+    const bool last_on = lane < nch - 32 * (ipr - 1);
+    if (sl > 0)   // this warp's ring is free: the previous slice's items are consumed
+      stream_prologue<N, MODE>(prod, p, r0, warp, lane, c0, ipr, nrw, last_on, ring16, ring8);
     __syncthreads();  // the previous slice's table is no longer read
 
     // ---- stage x of the slice (binary16, zero past cols), padded per chunk
@@ -529,60 +690,15 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
     __syncthreads();
 
     // ---- stream the warp's rows of this slice
-    int seg = 0;
-    for (int j = 0; j < nrw; ++j) {
-      const int lr = warp + kNW * j;
-      const int row = r0 + lr;
-      seg = seg_from<MODE>(p, seg, row);
-      const M1Seg& sg = p.seg[seg];
-      const bool g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
-      float acc = 0.0f;
-      uint32_t tb = lane_base;   // table slot of the item's chunk
-      for (int ci = 0; ci < ipr; ++ci, tb += kChunkSlotBytes) {
-        const uint32_t so = (uint32_t)(st * kStage);
-        cp_wait<kS - 1>();   // this lane's copies of this item landed
-        const bool valid = ci < lane_items;
-        const uint4 v = lds128(ring16 + so);
-        uint2 ix = lds64(ring8 + so + kIdxOff);
-        if constexpr (kChecked && N == 2) {
-          if (valid && (bad_codes24(ix.x) | bad_codes24(ix.y))) {
-            report_checked(p.err);
-            ix = make_uint2(0x44444444u, 0x44444444u);
-          }
-        }
-        const uint2 s2 = lds64(ring8 + so + kSzOff);
-        const uint32_t sa = valid ? s2.x : 0u;   // ragged slice: zero contribution
-        const uint32_t sb = valid ? s2.y : 0u;
-        // refill the stage this lane just read with the item kS ahead
-        if (more) {
-          prod.issue(ring16 + so, ring8 + so);
-          more = prod.advance(p, r0, warp, nrw, lane);
-        }
-        cp_commit();
-        st = st + 1 == kS ? 0 : st + 1;
-        if constexpr (N == 1 && MODE == kMany) {
-          if (g64)
-            acc = chunk_dot<N, true>(v, ix, sa, sb, tb, magic, acc);
-          else
-            acc = chunk_dot<N, false>(v, ix, sa, sb, tb, magic, acc);
-        } else {
-          acc = chunk_dot<N, N == 1 && MODE == kOneG64>(v, ix, sa, sb, tb, magic, acc);
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (lane == 0) {
-        __half* yrow = sg.y + (row - sg.row_begin);
-        if (p.nslices == 1) {
-          *yrow = __float2half_rn(acc);
-        } else {
-          const float t = (sl ? part[lr] : 0.0f) + acc;
-          if (sl == p.nslices - 1)
-            *yrow = __float2half_rn(t);
-          else
-            part[lr] = t;
-        }
-      }
+    c.c0 = c0;
+    c.last_on = last_on;
+    c.par = 0;
+    switch (ipr) {
+      case 1: stream_slice<N, MODE, 1>(c, r0, warp, sl, part); break;
+      case 2: stream_slice<N, MODE, 2>(c, r0, warp, sl, part); break;
+      case 3: if constexpr (max_ipr<N>() >= 3) stream_slice<N, MODE, 3>(c, r0, warp, sl, part); break;
+      case 4: if constexpr (max_ipr<N>() >= 4) stream_slice<N, MODE, 4>(c, r0, warp, sl, part); break;
+      default: break;   // the plan never makes more
     }
   }
   cp_wait<0>();  // no copy outstanding when the CTA retires
@@ -609,7 +725,10 @@ __global__ void __launch_bounds__(kNT, 1) k_m1_dual(const __grid_constant__ M1Du
 
 // Time of a 1:4 chunk against a 2:4 chunk in the M=1 kernel (a CTA-time
 // trace of the mixed q/k/v launch; 1.3 gave the shortest step of 1.0-1.5)
-constexpr double kCost14 = 1.3;
+#ifndef SGEMV_M1_COST14
+#define SGEMV_M1_COST14 1.3
+#endif
+constexpr double kCost14 = SGEMV_M1_COST14;
 
 int g_num_sms[64] = {0};
 
@@ -649,7 +768,7 @@ cudaError_t plan_m1(const Layout* Ls, const RunArgs* as, int count, int ctas, M1
   const size_t ring = (size_t)kNW * kS * kStage;
   const size_t part_max = 4096;   // rows_per_cta <= 1024 when K is sliced
   const size_t room = kSmemLimit - kTabAlign - ring - part_max;
-  const int max_cpl = (int)(room / (C::TAB_PER_CPL + C::X_PER_CPL));
+  const int max_cpl = min((int)(room / (C::TAB_PER_CPL + C::X_PER_CPL)), max_ipr<N>());
   if (max_cpl < 1) return cudaErrorNotSupported;
   const int nslices = (chunks + 32 * max_cpl - 1) / (32 * max_cpl);
   const int cpl = (chunks + 32 * nslices - 1) / (32 * nslices);
