@@ -785,9 +785,25 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+def layer_groups(gvs):
+    """Index groups of matrices that share x in a decoder layer (q/k/v,
+    gate/up; the others alone), by name, for the matrices present."""
+    pos = {g.name: i for i, g in enumerate(gvs)}
+    groups, seen = [], set()
+    for grp in GROUPS:
+        idx = [pos[n] for n in grp if n in pos]
+        if idx:
+            groups.append(idx)
+            seen.update(idx)
+    groups += [[i] for i in range(len(gvs)) if i not in seen]
+    return groups
+
+
 def run_batch_sweep(args, swo, dev, stream, l2, gvs=None, ms=None):
     """us and GB/s per M for the config-4 set (seven 2:4 g128 matrices), or
-    for the given matrices and M values."""
+    for the given matrices and M values: the grouped step (run_group over
+    q/k/v and gate/up, as the decode step) and, beside it, one call per
+    matrix (us_per_step_calls)."""
     import torch
     gvs = synth.config4(args.seed) if gvs is None else gvs
     ms = synth.CONFIG4_M if ms is None else ms
@@ -813,36 +829,56 @@ def run_batch_sweep(args, swo, dev, stream, l2, gvs=None, ms=None):
             cp.append(h)
         sets.append(cp)
     sptr = stream.cuda_stream
+    groups = layer_groups(gvs)
     out = {}
     for m in ms:
-        xs = [torch.from_numpy(gv.x(m)).to(dev) for gv in gvs]
+        xs = [None] * len(gvs)
+        for grp in groups:
+            x0 = torch.from_numpy(gvs[grp[0]].x(m)).to(dev)
+            for i in grp:
+                xs[i] = x0
         ys = [torch.empty((m, gv.rows), dtype=torch.float16, device=dev) for gv in gvs]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            for h, x, y in zip(sets[0], xs, ys):
-                h.run(x, y, sptr)
-            with torch.cuda.graph(g, stream=stream):
-                for k in range(copies):
-                    for h, x, y in zip(sets[k], xs, ys):
-                        h.run(x, y, sptr)
-        g.replay()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        reps = 5
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+
+        def step(st, grouped):
+            if grouped:
+                for grp in groups:
+                    if len(grp) == 1:
+                        st[grp[0]].run(xs[grp[0]], ys[grp[0]], sptr)
+                    else:
+                        swo.run_group([st[i] for i in grp], xs[grp[0]],
+                                      [ys[i] for i in grp], sptr)
+            else:
+                for h, x, y in zip(st, xs, ys):
+                    h.run(x, y, sptr)
+
+        res = {}
+        for grouped in (True, False):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                step(sets[0], grouped)
+                with torch.cuda.graph(g, stream=stream):
+                    for k in range(copies):
+                        step(sets[k], grouped)
+            g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            reps = 5
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            res[grouped] = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+            del g
+        us = res[True]
         b = step_bytes(gvs, m)
         fl = sum(gv.flops(m) for gv in gvs)
         out[str(m)] = {"us_per_step": round(us, 3), "gbs": round(b / us / 1e3, 1),
                        "tflops": round(fl / us / 1e6, 2),
-                       "us_per_call": round(us / len(gvs), 3)}
-        del g
+                       "launches_per_step": len(groups),
+                       "us_per_step_calls": round(res[False], 3)}
     for st in sets:
         for h in st:
             h.close()

@@ -190,8 +190,14 @@ int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
  * launch -- at most 8 of each N; the CTAs of one part take the 2:4 matrices
  * and those of the other the 1:4 ones, in proportion to their packed bytes,
  * and each CTA stages x and its lookup table once for all of its matrices
- * (more than 8 of one N: one launch per N and per 8); with m > 1 each matrix
- * runs as in sgemv_run.
+ * (more than 8 of one N: one launch per N and per 8).  With 2 <= m <= 16 the
+ * matrices of one N share a launch of the batch kernel (at most 8 per
+ * launch) when their row tiles still leave room to split K across a
+ * cluster, else each runs alone; the outputs then match a single run within
+ * the same tolerance, but the order of the fp32 partial sums may differ.
+ * A device-side error of a shared launch (a bounded wait that ran out) is
+ * recorded in the status word of the launch's first handle.  With m > 16
+ * each matrix runs as in sgemv_run.
  *   handles : count packed handles on one device, all with the same cols;
  *             n_keep and group may differ;
  *   x_dev   : m x cols binary16, 16-byte aligned, shared by all;

@@ -145,6 +145,9 @@ struct RunArgs {
 // Each returns cudaErrorNotSupported when it does not cover the case.
 cudaError_t launch_m1(const Layout& L, const RunArgs& a, cudaStream_t s);
 cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s);
+// 2 <= m <= 64 over up to 8 matrices sharing x, cols, N and m in one launch
+// of the warp-level sparse MMA kernel (errors go to as[0].err).
+cudaError_t launch_mma_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s);
 // m = 1 over several matrices sharing x, cols and N in one launch.
 cudaError_t launch_m1_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s);
 // m = 1 over 2:4 matrices (L2, n2) and 1:4 matrices (L1, n1) sharing x, in

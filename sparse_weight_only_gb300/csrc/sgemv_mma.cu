@@ -22,10 +22,11 @@
 //    half) and g + 8 (high half), one PRMT of the two rows' code words.
 //  * B (32 x 8): x rows staged in shared memory (padded rows, so ldmatrix
 //    reads are conflict-free), one ldmatrix.x4 per n-tile and k-tile.
-//  * weights: the CTA's 128 rows x K sub-slice (codes, positions and the
-//    sub-slice's scale/zero words) are copied into shared memory with
-//    cp.async, double-buffered across sub-slices; the first sub-slice is in
-//    flight while x is staged.  Warps read their rows from padded rows of
+//  * weights and x: the CTA's 128 rows x K sub-slice (codes, positions and
+//    the sub-slice's scale/zero words) and the sub-slice's x columns are
+//    copied into shared memory with cp.async, double-buffered across
+//    sub-slices; the first sub-slice's weights are in flight before the
+//    wait for the previous kernel.  Warps read their rows from padded rows of
 //    the buffer (conflict-free).
 //  * scale: each k-tile lies inside one group; the MMA accumulates a group
 //    into a temporary that is scaled by s and added in fp32.
@@ -36,6 +37,8 @@
 //    (one split cluster barrier, arrive at launch and wait after the main
 //    loop, orders the setup); wider tiles are written to each CTA's shared
 //    memory and pulled by the owners between two cluster barriers.
+#include <string.h>
+
 #include <cooperative_groups.h>
 
 #include "sgemv_internal.cuh"
@@ -52,11 +55,27 @@ constexpr int kRowsCta = 16 * kW;     // weight rows per CTA
 #endif
 constexpr int kMaxSplit = SGEMV_MMA_MAXSPLIT;  // CTAs per cluster (portable limit 8)
 constexpr size_t kSmemPerCta = 113 * 1024;  // two CTAs per SM
+constexpr int kCtasPerSm = 2;
 #ifndef SGEMV_MMA_PDL
 #define SGEMV_MMA_PDL 1
 #endif
 
+// One packed matrix of a launch: a launch covers up to kMaxSegs matrices
+// that share x, cols and N; their 128-row tiles are numbered in order.
+constexpr int kMaxSegs = 8;
+struct MmaSeg {
+  const uint4* vals;
+  const uint2* idx;
+  const uint32_t* sz;
+  __half* y;
+  int rows, gstride, gshift, ngroups;
+  int tile_begin;     // first row tile of this matrix in the launch
+};
+
 struct MmaParams {
+  MmaSeg seg[kMaxSegs];
+  int nseg;
+  // the CTA's matrix (copied from seg[] at the start of the kernel)
   const uint4* vals;
   const uint2* idx;
   const uint32_t* sz;
@@ -69,6 +88,7 @@ struct MmaParams {
   int sub_chunks;     // chunks of weights and x staged at a time
   int sub_groups;     // scale/zero words per row staged per sub-slice (bound)
   int ngroups;        // scale/zero groups per row
+  int row_tile0;      // (the CTA's matrix) its first tile in the launch
   int* err;           // device error word (a bounded wait that gave up)
   // Failure-detection test hook (0 in normal use): every rank withholds its
   // split-K partials, so each owner's bounded wait runs out after wait_ns.
@@ -110,6 +130,12 @@ __device__ __forceinline__ void cp_async(uint32_t dst, const void* src) {
   else
     asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(BYTES)
                  : "memory");
+}
+// 16 bytes, of which the first `src_bytes` (0 or 16) come from src and the
+// rest are zero
+__device__ __forceinline__ void cp_async_zfill(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -283,10 +309,11 @@ __device__ __forceinline__ void stage_weights(const MmaParams& p, const WGeom& W
 }
 
 template <int NT, int N>
-__global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
+__global__ void __launch_bounds__(kW * 32, 2) k_mma24(const __grid_constant__ MmaParams pp) {
   constexpr int CPC = N == 2 ? 64 : 128;   // dense columns per chunk
   constexpr int KT = CPC / 32;             // MMA k-steps per chunk
   extern __shared__ __align__(128) unsigned char smem[];
+  MmaParams p = pp;   // scalars; the CTA's matrix is filled in below
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -294,21 +321,37 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   const int mp = NT * 8;                       // padded activation rows
   const int xs_stride = p.sub_chunks * CPC + 8; // halves per staged x row
   const WGeom W(p.sub_chunks, p.sub_groups);
-  // shared memory: x of the sub-slice | two weight buffers | (pushed
+  // shared memory: x of two sub-slices | two weight buffers | (pushed
   // reduction) the receive buffer, one slot of ceil(R / nsplit) rows x mp
-  // per rank, and its mbarrier.  The pulled reduction writes its partial
-  // tile over the front once the main loop is done.
-  __half* xs = reinterpret_cast<__half*>(smem);
-  const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(xs);
+  // per rank, and its mbarrier.  Sub-slice s uses x and weight buffer s & 1.
+  // The pulled reduction writes its partial tile over the front once the
+  // main loop is done.
+  const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(smem);
   const int xs_bytes = (mp * xs_stride * 2 + 127) & ~127;
-  const uint32_t wbuf0 = xs_s + (uint32_t)xs_bytes;
+  const uint32_t wbuf0 = xs_s + (uint32_t)(2 * xs_bytes);
   float* part = reinterpret_cast<float*>(smem);
   const int rq = (kRowsCta + p.nsplit - 1) / p.nsplit;
   const uint32_t recv_s = wbuf0 + (uint32_t)(2 * W.bytes);
   const uint32_t rbar = recv_s + (uint32_t)(p.nsplit * rq * mp * 4);
   const float* recv = reinterpret_cast<const float*>(smem + (recv_s - xs_s));
 
-  const int row0 = (blockIdx.x / p.nsplit) * kRowsCta;
+  // the matrix of this CTA's row tile
+  const int tile = (int)blockIdx.x / p.nsplit;
+  {
+    int si = 0;
+    while (si + 1 < pp.nseg && tile >= pp.seg[si + 1].tile_begin) ++si;
+    const MmaSeg& sg = pp.seg[si];
+    p.vals = sg.vals;
+    p.idx = sg.idx;
+    p.sz = sg.sz;
+    p.y = sg.y;
+    p.rows = sg.rows;
+    p.gstride = sg.gstride;
+    p.gshift = sg.gshift;
+    p.ngroups = sg.ngroups;
+    p.row_tile0 = sg.tile_begin;
+  }
+  const int row0 = (tile - p.row_tile0) * kRowsCta;
   const int rowbase = row0 + warp * 16;
   const int rg = rowbase + g, rg8 = rowbase + g + 8;
   const bool vg = rg < p.rows, vg8 = rg8 < p.rows;
@@ -348,7 +391,17 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   }
 
-  // weights of the first sub-slice: in flight while x is staged
+  // x[:, CPC cs .. CPC ce) into x buffer xb, zero for padded rows (cols is a
+  // multiple of the group, so no 16-byte piece crosses the end of a row)
+  auto stage_x = [&](uint32_t xb, int cs, int ce) {
+    for (Walk2D w((ce - cs) * (CPC / 8)); w.r < mp; w.step()) {
+      const int col = cs * CPC + w.c * 8;
+      const bool in = w.r < p.m && col < p.cols;
+      cp_async_zfill(xb + (uint32_t)((w.r * xs_stride + w.c * 8) * 2),
+                     in ? p.x + (size_t)w.r * p.cols + col : p.x, in ? 16 : 0);
+    }
+  };
+  // weights of the first sub-slice: in flight while the previous kernel ends
   if (nsub > 0) {
     const int ce = min(c_end, c_begin + p.sub_chunks);
     stage_weights(p, W, wbuf0, row0, c_begin, ce, (c_begin * CPC) >> p.gshift,
@@ -358,31 +411,27 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
   // x may be written by the previous kernel: wait for it only now
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
+  if (nsub > 0) stage_x(xs_s, c_begin, min(c_end, c_begin + p.sub_chunks));
+  cp_commit();
 
   for (int sidx = 0; sidx < nsub; ++sidx) {
     const int cs = c_begin + sidx * p.sub_chunks;
     const int ce = min(c_end, cs + p.sub_chunks);
     const int g0 = (cs * CPC) >> p.gshift;
     const uint32_t wb = wbuf0 + (uint32_t)((sidx & 1) * W.bytes);
-    __syncthreads();  // previous sub-slice fully consumed: x and the other buffer are free
+    const uint32_t ld_x = ld_base + (uint32_t)((sidx & 1) * xs_bytes);
+    __syncthreads();  // previous sub-slice fully consumed: the other buffers are free
     if (sidx + 1 < nsub) {
+      // the next sub-slice's weights and x, in flight during this one
       const int ns = ce, ne = min(c_end, ns + p.sub_chunks);
-      stage_weights(p, W, wbuf0 + (uint32_t)(((sidx + 1) & 1) * W.bytes), row0, ns, ne,
+      const int nb = (sidx + 1) & 1;
+      stage_weights(p, W, wbuf0 + (uint32_t)(nb * W.bytes), row0, ns, ne,
                     (ns * CPC) >> p.gshift, min(p.ngroups - 1, (ne * CPC - 1) >> p.gshift));
+      stage_x(xs_s + (uint32_t)(nb * xs_bytes), ns, ne);
     }
     cp_commit();
-    {
-      // stage x[:, CPC cs .. CPC ce) (zero for padded rows and past cols)
-      for (Walk2D w((ce - cs) * (CPC / 8)); w.r < mp; w.step()) {
-        uint4 q = make_uint4(0, 0, 0, 0);
-        const int col = cs * CPC + w.c * 8;
-        if (w.r < p.m && col < p.cols)
-          q = *reinterpret_cast<const uint4*>(p.x + (size_t)w.r * p.cols + col);
-        *reinterpret_cast<uint4*>(xs + w.r * xs_stride + w.c * 8) = q;
-      }
-    }
     cp_wait<1>();     // this thread's copies of sub-slice sidx landed
-    __syncthreads();  // ... and every thread's; x is staged
+    __syncthreads();  // ... and every thread's
     for (int c = cs; c < ce; ++c) {
       const int cc = c - cs;
       uint4 v_g = make_uint4(0, 0, 0, 0), v_g8 = v_g;
@@ -460,7 +509,7 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(MmaParams p) {
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(ld_base + (uint32_t)(n * 8 * xs_stride * 2) + kofs, b0, b1, b2, b3);
+          ldsm_x4(ld_x + (uint32_t)(n * 8 * xs_stride * 2) + kofs, b0, b1, b2, b3);
           mma_sp(tmp[n], a0, a1, a2, a3, b0, b1, b2, b3, meta);
         }
       }
@@ -576,7 +625,7 @@ size_t mma_smem(int nt, int sc, int group, int cpc, int nsplit) {
   const int mp = nt * 8;
   const WGeom W(sc, (sc * cpc + group - 1) / group + 1);
   const size_t xs = ((size_t)mp * (sc * cpc + 8) * 2 + 127) & ~(size_t)127;
-  const size_t main = xs + 2 * (size_t)W.bytes;
+  const size_t main = 2 * xs + 2 * (size_t)W.bytes;
   if (!push_reduce(nt)) {
     const size_t red = (size_t)kRowsCta * mp * 4;
     return main > red ? main : red;
@@ -585,42 +634,53 @@ size_t mma_smem(int nt, int sc, int group, int cpc, int nsplit) {
   return main + recv + 16;
 }
 
+// One launch over `count` matrices that share x, cols, N and m.
 template <int NT, int N>
-cudaError_t launch_nt(const Layout& L, const RunArgs& a, cudaStream_t s, int sms) {
+cudaError_t launch_nt(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s, int sms) {
   constexpr int CPC = N == 2 ? 64 : 128;
-  const int chunks = (int)L.chunks;
-  const int ntiles = (L.rows + kRowsCta - 1) / kRowsCta;
-#ifndef SGEMV_MMA_CTAS_PER_SM
-#define SGEMV_MMA_CTAS_PER_SM 2
-#endif
+  const Layout& L0 = Ls[0];
+  const RunArgs& a = as[0];
+  const int chunks = (int)L0.chunks;
+  int ntiles = 0, gmin = 256;
+  MmaParams p;
+  memset(&p, 0, sizeof p);
+  for (int i = 0; i < count; ++i) {
+    MmaSeg& sg = p.seg[i];
+    sg.vals = as[i].vals;
+    sg.idx = as[i].idx;
+    sg.sz = as[i].sz;
+    sg.y = as[i].y;
+    sg.rows = Ls[i].rows;
+    sg.gstride = (int)Ls[i].gstride;
+    sg.gshift = Ls[i].group == 64 ? 6 : (Ls[i].group == 128 ? 7 : 8);
+    sg.ngroups = (int)Ls[i].ngroups;
+    sg.tile_begin = ntiles;
+    ntiles += (Ls[i].rows + kRowsCta - 1) / kRowsCta;
+    gmin = min(gmin, Ls[i].group);
+  }
+  for (int i = count; i < kMaxSegs; ++i) p.seg[i].tile_begin = ntiles;
+  p.nseg = count;
+  if (ntiles == 0) return cudaSuccess;
   // as many K splits as keep every CTA resident in one wave
-  int nsplit = (SGEMV_MMA_CTAS_PER_SM * sms) / ntiles;
+  int nsplit = (kCtasPerSm * sms) / ntiles;
   nsplit = max(1, min(kMaxSplit, min(nsplit, chunks)));
   const int split_chunks = (chunks + nsplit - 1) / nsplit;
   nsplit = (chunks + split_chunks - 1) / split_chunks;
-  // sub-slices: as many chunks as fit two CTAs per SM
+  // sub-slices: as many chunks as fit two CTAs per SM (the smallest group
+  // has the most scale/zero words per sub-slice)
   int sub = min(split_chunks, 64);
-  while (sub > 1 && mma_smem(NT, sub, L.group, CPC, nsplit) > kSmemPerCta) sub = (sub + 1) / 2;
-  const size_t smem = mma_smem(NT, sub, L.group, CPC, nsplit);
+  while (sub > 1 && mma_smem(NT, sub, gmin, CPC, nsplit) > kSmemPerCta) sub = (sub + 1) / 2;
+  const size_t smem = mma_smem(NT, sub, gmin, CPC, nsplit);
   if (smem > 227 * 1024) return cudaErrorNotSupported;
-  MmaParams p;
-  p.vals = a.vals;
-  p.idx = a.idx;
-  p.sz = a.sz;
   p.x = a.x;
-  p.y = a.y;
-  p.rows = L.rows;
-  p.cols = L.cols;
-  p.gstride = (int)L.gstride;
-  p.cstride = (int)L.cstride;
-  p.gshift = L.group == 64 ? 6 : (L.group == 128 ? 7 : 8);
+  p.cols = L0.cols;
+  p.cstride = (int)L0.cstride;
   p.chunks = chunks;
   p.m = a.m;
   p.split_chunks = split_chunks;
   p.nsplit = nsplit;
   p.sub_chunks = sub;
-  p.sub_groups = (sub * CPC + L.group - 1) / L.group + 1;
-  p.ngroups = (int)L.ngroups;
+  p.sub_groups = (sub * CPC + gmin - 1) / gmin + 1;
   p.err = a.err;
   p.withhold = a.withhold;
   p.wait_ns = a.withhold ? kInjectWaitNs : kWaitLimitNs;
@@ -664,9 +724,14 @@ bool withhold_applies(const Layout& L, int m) {
   return m >= 2 && L.rows > 0 && L.cols > 0;
 }
 
-cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s) {
-  if (a.m < 2 || a.m > 64 || L.rows == 0 || L.cols == 0)
-    return cudaErrorNotSupported;
+cudaError_t launch_mma_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s) {
+  if (count < 1 || count > kMaxSegs) return cudaErrorNotSupported;
+  const int m = as[0].m;
+  for (int i = 0; i < count; ++i)
+    if (as[i].m != m || Ls[i].cols != Ls[0].cols || Ls[i].n_keep != Ls[0].n_keep ||
+        Ls[i].rows == 0 || Ls[i].cols == 0)
+      return cudaErrorNotSupported;
+  if (m < 2 || m > 64) return cudaErrorNotSupported;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
   if (!g_sms[dev]) {
@@ -675,30 +740,49 @@ cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s) {
       return cudaErrorNotSupported;
     g_sms[dev] = n;
   }
-  const int nt = (a.m + 7) / 8;
+  const int nt = (m + 7) / 8;
   const int sms = g_sms[dev];
-  if (L.n_keep == 2) {
+  if (count > 1) {
+    int ntiles = 0;
+    for (int i = 0; i < count; ++i) ntiles += (Ls[i].rows + kRowsCta - 1) / kRowsCta;
+    if (kCtasPerSm * sms / ntiles < 2) {
+      // one launch could not split K: each CTA would walk a whole row of
+      // sub-slices; separate launches, each split, measured faster
+      for (int i = 0; i < count; ++i) {
+        const cudaError_t e = launch_mma_group(Ls + i, as + i, 1, s);
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+  }
+  if (Ls[0].n_keep == 2) {
     switch (nt) {
-      case 1: return launch_nt<1, 2>(L, a, s, sms);
-      case 2: return launch_nt<2, 2>(L, a, s, sms);
-      case 3: return launch_nt<3, 2>(L, a, s, sms);
-      case 4: return launch_nt<4, 2>(L, a, s, sms);
-      case 5: return launch_nt<5, 2>(L, a, s, sms);
-      case 6: return launch_nt<6, 2>(L, a, s, sms);
-      case 7: return launch_nt<7, 2>(L, a, s, sms);
-      default: return launch_nt<8, 2>(L, a, s, sms);
+      case 1: return launch_nt<1, 2>(Ls, as, count, s, sms);
+      case 2: return launch_nt<2, 2>(Ls, as, count, s, sms);
+      case 3: return launch_nt<3, 2>(Ls, as, count, s, sms);
+      case 4: return launch_nt<4, 2>(Ls, as, count, s, sms);
+      case 5: return launch_nt<5, 2>(Ls, as, count, s, sms);
+      case 6: return launch_nt<6, 2>(Ls, as, count, s, sms);
+      case 7: return launch_nt<7, 2>(Ls, as, count, s, sms);
+      default: return launch_nt<8, 2>(Ls, as, count, s, sms);
     }
   }
   switch (nt) {
-    case 1: return launch_nt<1, 1>(L, a, s, sms);
-    case 2: return launch_nt<2, 1>(L, a, s, sms);
-    case 3: return launch_nt<3, 1>(L, a, s, sms);
-    case 4: return launch_nt<4, 1>(L, a, s, sms);
-    case 5: return launch_nt<5, 1>(L, a, s, sms);
-    case 6: return launch_nt<6, 1>(L, a, s, sms);
-    case 7: return launch_nt<7, 1>(L, a, s, sms);
-    default: return launch_nt<8, 1>(L, a, s, sms);
+    case 1: return launch_nt<1, 1>(Ls, as, count, s, sms);
+    case 2: return launch_nt<2, 1>(Ls, as, count, s, sms);
+    case 3: return launch_nt<3, 1>(Ls, as, count, s, sms);
+    case 4: return launch_nt<4, 1>(Ls, as, count, s, sms);
+    case 5: return launch_nt<5, 1>(Ls, as, count, s, sms);
+    case 6: return launch_nt<6, 1>(Ls, as, count, s, sms);
+    case 7: return launch_nt<7, 1>(Ls, as, count, s, sms);
+    default: return launch_nt<8, 1>(Ls, as, count, s, sms);
   }
+}
+
+cudaError_t launch_mma(const Layout& L, const RunArgs& a, cudaStream_t s) {
+  if (a.m < 2 || a.m > 64 || L.rows == 0 || L.cols == 0)
+    return cudaErrorNotSupported;
+  return launch_mma_group(&L, &a, 1, s);
 }
 
 }  // namespace sgemv

@@ -1,5 +1,9 @@
-"""Grouped run (several matrices sharing x) through the C ABI: every output
-equals the per-matrix run bit for bit and matches the oracle."""
+"""Grouped run (several matrices sharing x) through the C ABI.  Every output
+matches the oracle; at m = 1 it also equals the per-matrix run bit for bit
+(each row is computed the same way in either launch).  At 2 <= m <= 16 the
+matrices of one N share a launch of the sparse MMA kernel, whose split of K
+across a cluster depends on the launch's tile count, so there the summation
+order -- not the tolerance -- may differ from a single run."""
 import numpy as np
 import pytest
 
@@ -35,9 +39,11 @@ SPECS_MANY = [(40 + 7 * i, 1, (64, 128, 256)[i % 3]) for i in range(9)] + \
 
 
 @pytest.mark.parametrize("m,cols,specs", [(1, 1536, SPECS_MIXED), (5, 1536, SPECS_MIXED),
-                                          (1, 8192, SPECS_MIXED), (1, 1024, SPECS_MANY)])
+                                          (1, 8192, SPECS_MIXED), (1, 1024, SPECS_MANY),
+                                          (2, 1536, SPECS_MIXED), (16, 1536, SPECS_MIXED),
+                                          (9, 1024, SPECS_MANY), (24, 1536, SPECS_MIXED)])
 def test_group_matches_single_and_oracle(native, orc, m, cols, specs):
-    mats = _mats(native, orc, specs, cols, max_m=8)
+    mats = _mats(native, orc, specs, cols, max_m=24)
     x = torch.from_numpy(synth.activations(41 + m, m, cols)).cuda()
     ys = _ys(mats, m)
     native.run_group([h for h, _ in mats], x, ys)
@@ -46,34 +52,41 @@ def test_group_matches_single_and_oracle(native, orc, m, cols, specs):
         single = torch.empty_like(y)
         h.run(x, single)
         torch.cuda.synchronize()
-        assert torch.equal(y, single)
+        if m == 1 or m > 16:
+            assert torch.equal(y, single)
         ref = orc.matvec(p, x.cpu().numpy())
         norms = np.abs(orc.dequant(p)).sum(axis=1)
-        check_y(orc, y.cpu().numpy(), ref, norms, f"group member {h.rows}x{cols}")
+        check_y(orc, y.cpu().numpy(), ref, norms, f"group member {h.rows}x{cols} m={m}")
+        check_y(orc, single.cpu().numpy(), ref, norms, f"single {h.rows}x{cols} m={m}")
         assert h.status() == 0
 
 
-def test_group_qkv_shapes(native, orc):
-    """The decoder layer's q/k/v (mixed N, g) and gate/up groups at full size."""
-    gvs = synth.config3()
+@pytest.mark.parametrize("config,m", [("config3", 1), ("config4", 4), ("config4", 16),
+                                      ("config3", 8)])
+def test_group_qkv_shapes(native, orc, config, m):
+    """The decoder layer's q/k/v (mixed N, g in the layer set; all 2:4 g128 in
+    the verification-batch set) and gate/up groups at full size."""
+    gvs = getattr(synth, config)()
     for names in (("q", "k", "v"), ("gate", "up")):
         sel = [g for g in gvs if g.name in names]
         mats = []
         for gv in sel:
             W = gv.weight()
             p = orc.pack(W, gv.n_keep, gv.group)
-            h = native.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group)
+            h = native.SparseGemv(gv.rows, gv.cols, gv.n_keep, gv.group, max_m=m)
             h.pack(W)
             mats.append((h, p))
-        x = torch.from_numpy(sel[0].x(1)).cuda()
-        ys = _ys(mats, 1)
+        x = torch.from_numpy(sel[0].x(m)).cuda()
+        ys = _ys(mats, m)
         native.run_group([h for h, _ in mats], x, ys)
         torch.cuda.synchronize()
         for (h, p), y in zip(mats, ys):
             single = torch.empty_like(y)
             h.run(x, single)
             torch.cuda.synchronize()
-            assert torch.equal(y, single)
+            if m == 1:
+                assert torch.equal(y, single)
+            assert h.status() == 0
             rows = np.arange(0, h.rows, 37, dtype=np.int64)
             ref = orc.matvec(p, x.cpu().numpy(), rows)
             norms = np.array([np.abs(orc.dequant(p, int(r), 1)).sum() for r in rows])
