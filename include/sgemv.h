@@ -196,8 +196,10 @@ int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
  * cluster, else each runs alone; the outputs then match a single run within
  * the same tolerance, but the order of the fp32 partial sums may differ.
  * A device-side error of a shared launch (a bounded wait that ran out) is
- * recorded in the status word of the launch's first handle.  With m > 16
- * each matrix runs as in sgemv_run.
+ * recorded in the status word of the launch's first handle.  With
+ * 17 <= m <= 64 the matrices of one N and group size share a launch of the
+ * tensor-core batch kernel (at most 4 per launch; the split-K partials use
+ * the first handle's workspace).
  *   handles : count packed handles on one device, all with the same cols;
  *             n_keep and group may differ;
  *   x_dev   : m x cols binary16, 16-byte aligned, shared by all;

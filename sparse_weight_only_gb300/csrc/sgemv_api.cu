@@ -562,9 +562,48 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
   if (m != 1) {
     bool hook = false;
     for (int i = 0; i < count; ++i) hook = hook || handles[i]->withhold_runs > 0;
-    if (m > sgemv::kMmaSyncMaxM || hook) {
+    if (hook) {
       for (int i = 0; i < count; ++i)
         if (int rc = run_checked(handles[i], x_dev, y_devs[i], m, s)) return rc;
+      return SGEMV_OK;
+    }
+    if (m > sgemv::kMmaSyncMaxM) {
+      // the tcgen05 kernel: one launch per (N, group size) and per
+      // tc_max_group() matrices
+      const int tcap = sgemv::tc_max_group();
+      for (int n = 1; n <= 2; ++n)
+        for (int gs = 64; gs <= 256; gs *= 2) {
+          sgemv::Layout Ls[8];
+          sgemv::RunArgs as[8];
+          const sgemv::TcMaps* maps[8];
+          int k = 0;
+          for (int i = 0; i <= count; ++i) {
+            if (i < count && handles[i]->L.n_keep == n && handles[i]->L.group == gs &&
+                handles[i]->L.rows > 0) {
+              sgemv_t h = handles[i];
+              Ls[k] = h->L;
+              as[k].vals = h->d_vals;
+              as[k].idx = h->d_idx;
+              as[k].sz = h->d_sz;
+              as[k].x = static_cast<const __half*>(x_dev);
+              as[k].y = static_cast<__half*>(y_devs[i]);
+              as[k].m = m;
+              as[k].err = h->d_err;
+              maps[k] = &h->tc;
+              ++k;
+            }
+            if (k > 0 && (k == tcap || i == count)) {
+              cudaError_t e = sgemv::launch_tc_group(Ls, as, maps, k, s, 1 << 30);
+              if (e == cudaErrorNotSupported) {
+                (void)cudaGetLastError();
+                return fail(SGEMV_ERR_UNSUPPORTED,
+                            "a grouped matrix is beyond the product kernels' 32-bit chunk index space");
+              }
+              if (e != cudaSuccess) return cuda_fail(e, "grouped SparseGemv launch");
+              k = 0;
+            }
+          }
+        }
       return SGEMV_OK;
     }
     // 2 <= m <= 16: one launch of the sparse MMA kernel per N and per

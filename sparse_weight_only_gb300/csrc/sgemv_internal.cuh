@@ -164,6 +164,11 @@ cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cud
 // ... on at most max_ctas CTAs (a workspace sized for that many).
 cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s,
                       int max_ctas);
+// ... over up to tc_max_group() matrices sharing x, cols, N, the group size
+// and m in one launch (partials in maps[0]'s workspace; errors to as[0].err).
+int tc_max_group();
+cudaError_t launch_tc_group(const Layout* Ls, const RunArgs* as, const TcMaps* const* maps,
+                            int count, cudaStream_t s, int max_ctas);
 // Sets the calling thread's sgemv_last_error text; returns `code`
 // (report_cuda: SGEMV_ERR_CUDA with the runtime's message).
 int report(int code, const char* msg);

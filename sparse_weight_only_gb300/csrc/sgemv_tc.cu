@@ -60,13 +60,25 @@ constexpr int kSzWords = 8;            // scale/zero words per row and unit
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr unsigned long long kInjectWaitNs = 20000ull;
 
-struct TcParams {
-  CUtensorMap tm_vals, tm_idx, tm_sz, tm_x;
+// One packed matrix of a launch: a launch covers up to kTcMaxSeg matrices
+// that share x, cols, N and the group size; their 128-row tiles are
+// numbered in order.
+constexpr int kTcMaxSeg = 4;
+struct TcSeg {
+  CUtensorMap tm_vals, tm_idx, tm_sz;
   __half* y;
+  int* counters;         // [this matrix's tiles] arrivals per tile (left at 0)
+  int rows;
+  int tile_begin;        // first tile of this matrix in the launch
+};
+
+struct TcParams {
+  TcSeg seg[kTcMaxSeg];
+  CUtensorMap tm_x;
   float* scratch;        // [grid][2][128][npad] fp32 partial tiles
-  int* counters;         // [ntiles] arrivals per tile (left at 0)
   int* err;
-  int rows, cols, m;
+  int nseg;
+  int cols, m;
   int group, gshift;
   int ntiles, units_per_tile;
   long long total_units;
@@ -328,6 +340,28 @@ constexpr int kAlignPct = SGEMV_TC_ALIGN_PCT;   // least share of the SMs a tile
 #endif
 constexpr bool kClusterMode = SGEMV_TC_CLUSTER != 0;
 
+// The matrix of launch tile `tile`.
+__device__ __forceinline__ const TcSeg& seg_of(const TcParams& p, int tile) {
+  int s = 0;
+  while (s + 1 < p.nseg && tile >= p.seg[s + 1].tile_begin) ++s;
+  return p.seg[s];
+}
+// Row r of launch tile `tile` in its matrix's y (m x rows, row-major).
+struct YRow {
+  __half* y;
+  int rows, row;
+  __device__ __forceinline__ YRow(const TcParams& p, int tile, int r) {
+    const TcSeg& sg = seg_of(p, tile);
+    y = sg.y;
+    rows = sg.rows;
+    row = (tile - sg.tile_begin) * kRows + r;
+  }
+  __device__ __forceinline__ bool valid() const { return row < rows; }
+  __device__ __forceinline__ void put(int i, int m, float v) const {
+    if (i < m && row < rows) y[(size_t)i * rows + row] = __float2half_rn(v);
+  }
+};
+
 template <int N, int NPAD>
 __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcParams p) {
   constexpr int SUBS = N == 2 ? 2 : 4;           // sub-stages per unit
@@ -434,9 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
         mbar_expect_tx(bar, kStageW);
         const int chunk0 = w_uit * 4;
         const int g0 = ((w_uit * UNIT_COLS) >> p.gshift) & ~3;
-        tma_2d(dst + kValsOff, &p.tm_vals, chunk0 * 16, w_tile * kRows, bar);
-        tma_2d(dst + kIdxOff, &p.tm_idx, chunk0 * 8, w_tile * kRows, bar);
-        tma_2d(dst + kSzOff, &p.tm_sz, g0, w_tile * kRows, bar);
+        const TcSeg& sg = seg_of(p, w_tile);
+        const int wrow = (w_tile - sg.tile_begin) * kRows;
+        tma_2d(dst + kValsOff, &sg.tm_vals, chunk0 * 16, wrow, bar);
+        tma_2d(dst + kIdxOff, &sg.tm_idx, chunk0 * 8, wrow, bar);
+        tma_2d(dst + kSzOff, &sg.tm_sz, g0, wrow, bar);
         ++w_issued;
         if (++w_uit == U) {
           w_uit = 0;
@@ -533,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           // valid rows and columns only: the zero padding past the matrix
           // (rows of the last tile, columns past K) is never multiplied
           const int colv = uit * UNIT_COLS + ls * 128 + 64 * h;
-          const bool rowv = dtile * kRows + r < p.rows;
+          const bool rowv = YRow(p, dtile, r).valid();
           if (rowv && ((colv < p.cols && bad_codes24(m0)) || (colv + 32 < p.cols && bad_codes24(m1)))) {
             report_checked(p.err);
             m0 = m1 = 0x44444444u;
@@ -670,11 +706,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
         // ---- the segment is finished: y directly, or through the split-K
         // workspace when the tile is shared with other CTAs
         const int tile = wk.tile;
-        const int row = tile * kRows + r;
+        const YRow yr(p, tile, r);
         if (wk.seg_u0 == 0 && seg_u1 == U) {
 #pragma unroll
-          for (int i = 0; i < NPAD; ++i)
-            if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(acc[i]);
+          for (int i = 0; i < NPAD; ++i) yr.put(i, p.m, acc[i]);
         } else if (p.parts >= 2) {
           // cluster mode: the partial tile goes to this CTA's own shared
           // memory (the weight ring, free once every epilogue thread has read
@@ -699,13 +734,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           const long long tu0 = (long long)tile * U, tu1 = tu0 + U - 1;
           const int c0 = (int)(((tu0 + 1) * P - 1) / T), c1 = (int)(((tu1 + 1) * P - 1) / T);
           if (etid == 0) {
+            const TcSeg& sg = seg_of(p, tile);
+            int* ctr = sg.counters + (tile - sg.tile_begin);
             int old;
             asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
                          : "=r"(old)
-                         : "l"(p.counters + tile)
+                         : "l"(ctr)
                          : "memory");
             const bool done = old == c1 - c0;
-            if (done) p.counters[tile] = 0;   // left at 0 for the next launch
+            if (done) *ctr = 0;   // left at 0 for the next launch
             // the CTA's last segment: the whole CTA sums after its teardown
             // barrier (every role is finished then)
             const bool defer = done && ui + 1 == nunits;
@@ -733,8 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
               }
             }
 #pragma unroll
-            for (int i = 0; i < NPAD; ++i)
-              if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(sum[i]);
+            for (int i = 0; i < NPAD; ++i) yr.put(i, p.m, sum[i]);
           }
           asm volatile("bar.sync 1, 128;" ::: "memory");   // last_flag is read before it is reused
           first_seg = false;
@@ -799,13 +835,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
           const int it = it0 + k * kThreads;
           if (it >= kRows * G) continue;
           const int r = it / G, g = it % G;
-          const int row = ftile * kRows + r;
+          const YRow yr(p, ftile, r);
           const float o[4] = {s2[k].x, s2[k].y, s2[k].z, s2[k].w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = 4 * g + q;
-            if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(o[q]);
-          }
+          for (int q = 0; q < 4; ++q) yr.put(4 * g + q, p.m, o[q]);
         }
       }
     }
@@ -858,13 +891,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
             sum.w += v[k].w;
           }
       }
-      const int row = tile * kRows + r;
+      const YRow yr(p, tile, r);
       const float o[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = 4 * g + k;
-        if (i < p.m && row < p.rows) p.y[(size_t)i * p.rows + row] = __float2half_rn(o[k]);
-      }
+      for (int k = 0; k < 4; ++k) yr.put(4 * g + k, p.m, o[k]);
     }
     cluster_sync();
   }
@@ -939,31 +969,44 @@ size_t tc_smem(int npad) {
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
+// One launch over `count` matrices that share x, cols, N, the group size and
+// m; the split-K partials go to maps[0]'s workspace, each matrix's tile
+// arrivals to its own counters.
 template <int N, int NPAD>
-cudaError_t launch_tc_n(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s,
-                        int max_ctas) {
+cudaError_t launch_tc_n(const Layout* Ls, const RunArgs* as, const TcMaps* const* maps, int count,
+                        cudaStream_t s, int max_ctas) {
   constexpr int UNIT_COLS = N == 2 ? 256 : 512;
   const int sms = tc_sms();
   if (sms <= 0) return cudaErrorNotSupported;
+  const Layout& L = Ls[0];
+  const RunArgs& a = as[0];
   TcParams p;
   memset(&p, 0, sizeof p);
-  p.tm_vals = maps.vals;
-  p.tm_idx = maps.idx;
-  p.tm_sz = maps.sz;
+  int ntiles = 0;
+  for (int i = 0; i < count; ++i) {
+    TcSeg& sg = p.seg[i];
+    sg.tm_vals = maps[i]->vals;
+    sg.tm_idx = maps[i]->idx;
+    sg.tm_sz = maps[i]->sz;
+    sg.y = as[i].y;
+    sg.counters = maps[i]->counters;
+    sg.rows = Ls[i].rows;
+    sg.tile_begin = ntiles;
+    ntiles += (Ls[i].rows + kRows - 1) / kRows;
+  }
+  for (int i = count; i < kTcMaxSeg; ++i) p.seg[i].tile_begin = ntiles;
+  p.nseg = count;
   if (!encode_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x, (uint64_t)L.cols,
                  (uint64_t)a.m, 64, NPAD, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
     return cudaErrorInvalidValue;
-  p.y = a.y;
-  p.scratch = maps.scratch;
-  p.counters = maps.counters;
+  p.scratch = maps[0]->scratch;
   p.err = a.err;
-  p.rows = L.rows;
   p.cols = L.cols;
   p.m = a.m;
   p.group = L.group;
   p.gshift = L.group == 64 ? 6 : (L.group == 128 ? 7 : 8);
-  p.ntiles = (L.rows + kRows - 1) / kRows;
+  p.ntiles = ntiles;
   p.units_per_tile = (L.cols + UNIT_COLS - 1) / UNIT_COLS;
   p.total_units = (long long)p.ntiles * p.units_per_tile;
   const int cap = sms < max_ctas ? sms : max_ctas;
@@ -1056,25 +1099,39 @@ cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cud
 
 cudaError_t launch_tc(const Layout& L, const RunArgs& a, const TcMaps& maps, cudaStream_t s,
                       int max_ctas) {
+  const TcMaps* m[1] = {&maps};
+  return launch_tc_group(&L, &a, m, 1, s, max_ctas);
+}
+
+int tc_max_group() { return kTcMaxSeg; }
+
+cudaError_t launch_tc_group(const Layout* Ls, const RunArgs* as, const TcMaps* const* maps,
+                            int count, cudaStream_t s, int max_ctas) {
   if (max_ctas < 1) return cudaErrorInvalidValue;
-  if (a.m < 2 || a.m > 64 || L.rows == 0 || L.cols == 0 || !maps.ready || !maps.scratch ||
-      !maps.counters)
-    return cudaErrorNotSupported;
+  if (count < 1 || count > kTcMaxSeg) return cudaErrorNotSupported;
+  const Layout& L = Ls[0];
+  const RunArgs& a = as[0];
+  if (a.m < 2 || a.m > 64 || !maps[0]->scratch) return cudaErrorNotSupported;
+  for (int i = 0; i < count; ++i)
+    if (Ls[i].rows == 0 || Ls[i].cols != L.cols || Ls[i].cols == 0 ||
+        Ls[i].n_keep != L.n_keep || Ls[i].group != L.group || as[i].m != a.m ||
+        as[i].x != a.x || !maps[i]->ready || !maps[i]->counters)
+      return cudaErrorNotSupported;
   if (((uintptr_t)a.x & 15u) != 0) return cudaErrorNotSupported;
   const int np = npad_of(a.m);
   if (L.n_keep == 2) {
     switch (np) {
-      case 16: return launch_tc_n<2, 16>(L, a, maps, s, max_ctas);
-      case 32: return launch_tc_n<2, 32>(L, a, maps, s, max_ctas);
-      case 48: return launch_tc_n<2, 48>(L, a, maps, s, max_ctas);
-      default: return launch_tc_n<2, 64>(L, a, maps, s, max_ctas);
+      case 16: return launch_tc_n<2, 16>(Ls, as, maps, count, s, max_ctas);
+      case 32: return launch_tc_n<2, 32>(Ls, as, maps, count, s, max_ctas);
+      case 48: return launch_tc_n<2, 48>(Ls, as, maps, count, s, max_ctas);
+      default: return launch_tc_n<2, 64>(Ls, as, maps, count, s, max_ctas);
     }
   }
   switch (np) {
-    case 16: return launch_tc_n<1, 16>(L, a, maps, s, max_ctas);
-    case 32: return launch_tc_n<1, 32>(L, a, maps, s, max_ctas);
-    case 48: return launch_tc_n<1, 48>(L, a, maps, s, max_ctas);
-    default: return launch_tc_n<1, 64>(L, a, maps, s, max_ctas);
+    case 16: return launch_tc_n<1, 16>(Ls, as, maps, count, s, max_ctas);
+    case 32: return launch_tc_n<1, 32>(Ls, as, maps, count, s, max_ctas);
+    case 48: return launch_tc_n<1, 48>(Ls, as, maps, count, s, max_ctas);
+    default: return launch_tc_n<1, 64>(Ls, as, maps, count, s, max_ctas);
   }
 }
 
