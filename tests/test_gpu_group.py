@@ -41,6 +41,7 @@ SPECS_MANY = [(40 + 7 * i, 1, (64, 128, 256)[i % 3]) for i in range(9)] + \
 
 @pytest.mark.parametrize("m,cols,specs", [(1, 1536, SPECS_MIXED), (5, 1536, SPECS_MIXED),
                                           (1, 8192, SPECS_MIXED), (1, 1024, SPECS_MANY),
+                                          (1, 6144, SPECS_MIXED),
                                           (2, 1536, SPECS_MIXED), (16, 1536, SPECS_MIXED),
                                           (9, 1024, SPECS_MANY), (24, 1536, SPECS_MIXED),
                                           (64, 1536, SPECS_MIXED), (40, 1024, SPECS_MANY)])

@@ -62,6 +62,10 @@ SMALL = [  # rows, cols, n_keep, group, dist
     (40, 8192, 1, 256, "outliers"),
     (24, 16384, 2, 128, "outliers"),  # rows longer than one K slice
     (24, 16384, 1, 64, "normal"),
+    (70, 4160, 2, 64, "outliers"),    # M=1: three items per row, the last one lane wide
+    (33, 6144, 2, 128, "normal"),     # three full items per row
+    (20, 10240, 2, 256, "outliers"),  # K slices of three and two items per row
+    (17, 11008, 1, 128, "normal"),    # 1:4 K slices of two items and one ragged item
 ]
 
 
