@@ -641,62 +641,105 @@ def run_ours(args, rank, world, local):
         batch_mixed = run_batch_sweep(args, swo, dev, stream, l2, gvs, (4, 16, 64))
         rowg = run_rowgroup_case(args, swo, dev, stream, l2)
 
-    # end to end through the public host-buffer call: H2D x, kernels, D2H y
-    xh = [torch.from_numpy(gv.x(m)).pin_memory() for gv in gvs]
-    yh = [torch.empty((m, gv.rows), dtype=torch.float16).pin_memory() for gv in gvs]
+    # End to end, x from and y to page-locked host memory every step, two
+    # ways through the public API: (a) one copy of the step's activations
+    # in, the grouped device-buffer calls (sgemv_run_group over q/k/v and
+    # gate/up, sgemv_run for o and down: kernels back to back, as timed
+    # above), one copy of the outputs out -- the headline e2e; (b) the host-buffer calls
+    # sgemv_run_group_host / sgemv_run_host, whose copies sit between the
+    # kernels.  Each step is captured once per packed copy into a CUDA
+    # graph; a step is one replay on the benchmark's stream, a sync of that
+    # stream and a host read of y.
+    hgroups = layer_groups(gvs)
+    # the step's activations in one page-locked buffer and its outputs in
+    # one, so that each direction is one copy (views for the calls; every x
+    # view starts on a 128-byte boundary: cols is a multiple of 64)
+    xsz = {grp[0]: m * gvs[grp[0]].cols for grp in hgroups}
+    ysz = [m * gv.rows for gv in gvs]
+    xh_all = torch.empty(sum(xsz.values()), dtype=torch.float16).pin_memory()
+    xd_all = torch.empty_like(xh_all, device=dev)
+    yh_all = torch.empty(sum(ysz), dtype=torch.float16).pin_memory()
+    yd_all = torch.empty_like(yh_all, device=dev)
+    xh, xd, off = {}, {}, 0
+    for i, n in xsz.items():
+        xh[i] = xh_all[off:off + n].view(m, gvs[i].cols)
+        xh[i].copy_(torch.from_numpy(gvs[i].x(m)))
+        xd[i] = xd_all[off:off + n].view(m, gvs[i].cols)
+        off += n
+    yh, yd, off = [], [], 0
+    for gv, n in zip(gvs, ysz):
+        yh.append(yh_all[off:off + n].view(m, gv.rows))
+        yd.append(yd_all[off:off + n].view(m, gv.rows))
+        off += n
+    h2d_bytes = xh_all.numel() * xh_all.element_size()
+    d2h_bytes = yh_all.numel() * yh_all.element_size()
     lib = swo.load()
     e2e_steps = max(3, min(args.steps, 200))
 
-    def e2e_step(k):
-        for h, x, y in zip(sets[k % copies], xh, yh):
-            rc = lib.sgemv_run_host(h.handle, x.data_ptr(), y.data_ptr(), m, sptr)
-            if rc:
-                raise RuntimeError(lib.sgemv_last_error().decode())
-        stream.synchronize()
-        return float(yh[0][0, 0])
+    def e2e_issue_dev(st):
+        xd_all.copy_(xh_all, non_blocking=True)
+        for grp in hgroups:
+            if len(grp) == 1:
+                st[grp[0]].run(xd[grp[0]], yd[grp[0]], sptr)
+            else:
+                swo.run_group([st[i] for i in grp], xd[grp[0]], [yd[i] for i in grp], sptr)
+        yh_all.copy_(yd_all, non_blocking=True)
 
-    for k in range(3):
-        e2e_step(k)
-    barrier(world)
-    t0 = time.perf_counter()
-    for k in range(e2e_steps):
-        e2e_step(k)
-    t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
-    e2e_eager = sum_over_ranks(sb * e2e_steps, world, dev) / t_e2e / 1e9
+    def e2e_issue_host(st):
+        for grp in hgroups:
+            if len(grp) == 1:
+                i = grp[0]
+                rc = lib.sgemv_run_host(st[i].handle, xh[i].data_ptr(), yh[i].data_ptr(), m, sptr)
+                if rc:
+                    raise RuntimeError(lib.sgemv_last_error().decode())
+            else:
+                swo.run_group_host([st[i] for i in grp], xh[grp[0]], [yh[i] for i in grp], sptr)
 
-    # the same calls as a decode loop issues them: one step's seven
-    # sgemv_run_host calls (H2D of x, kernel, D2H of y each) captured once per
-    # packed copy, a graph launch per step, then a host sync and a read of y
-    e2e = e2e_eager
-    e2e_mode = "sgemv_run_host per matrix, eager, stream sync per step"
-    try:
+    def e2e_time(issue, graphed):
+        """GB/s of e2e_steps steps, each ending in a stream sync and a read of y."""
         graphs = []
-        for c in range(copies):
-            gh = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                with torch.cuda.graph(gh, stream=stream):
-                    for h, x, y in zip(sets[c], xh, yh):
-                        rc = lib.sgemv_run_host(h.handle, x.data_ptr(), y.data_ptr(), m, sptr)
-                        if rc:
-                            raise RuntimeError(lib.sgemv_last_error().decode())
-            graphs.append(gh)
+        if graphed:
+            for c in range(copies):
+                gh = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    with torch.cuda.graph(gh, stream=stream):
+                        issue(sets[c])
+                graphs.append(gh)
 
-        def e2e_graph_step(k):
-            graphs[k % copies].replay()
+        yv = yh_all.numpy()   # the host read of y, without tensor indexing
+
+        def one(k):
+            if graphed:
+                graphs[k % copies].replay()
+            else:
+                issue(sets[k % copies])
             stream.synchronize()
-            return float(yh[0][0, 0])
+            return float(yv[0])
 
-        for k in range(3):
-            e2e_graph_step(k)
-        barrier(world)
-        t0 = time.perf_counter()
-        for k in range(e2e_steps):
-            e2e_graph_step(k)
-        t_g = max_over_ranks(time.perf_counter() - t0, world, dev)
-        e2e = sum_over_ranks(sb * e2e_steps, world, dev) / t_g / 1e9
-        e2e_mode = ("sgemv_run_host per matrix captured in a CUDA graph per packed copy, "
-                    "one graph launch + stream sync + y read per step")
-        del graphs
+        # replay() launches on the current stream: make it the one each step
+        # is synchronised on, for the whole timed loop
+        with torch.cuda.stream(stream):
+            for k in range(3):
+                one(k)
+            barrier(world)
+            t0 = time.perf_counter()
+            for k in range(e2e_steps):
+                one(k)
+            t = time.perf_counter() - t0
+        t = max_over_ranks(t, world, dev)
+        return sum_over_ranks(sb * e2e_steps, world, dev) / t / 1e9
+
+    e2e_eager = e2e_time(e2e_issue_dev, False)
+    e2e = e2e_eager
+    e2e_mode = "one x copy in, sgemv_run_group / sgemv_run on device buffers, one y copy out; eager"
+    e2e_host = None
+    try:
+        e2e = e2e_time(e2e_issue_dev, True)
+        e2e_mode = ("one copy of the step's x in (pinned host -> device), run_group(q,k,v), "
+                    "run(o), run_group(gate,up), run(down) on device buffers, one copy of its y "
+                    "out; captured in a CUDA graph per packed copy, one replay + stream sync + "
+                    "y read per step")
+        e2e_host = e2e_time(e2e_issue_host, True)
     except Exception as exc:  # pragma: no cover - reported, the eager figure stands
         e2e_mode += f" (graph capture failed: {exc})"
 
@@ -756,9 +799,13 @@ def run_ours(args, rank, world, local):
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": traffic["bytes_per_step"] if traffic else None},
         "e2e": {"value": e2e, "unit": "GB/s",
-                "h2d_bytes_per_step": sum(2 * m * g.cols for g in gvs),
-                "d2h_bytes_per_step": sum(2 * m * g.rows for g in gvs),
-                "api": e2e_mode, "eager_value": e2e_eager},
+                "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes,
+                "api": e2e_mode, "eager_value": e2e_eager,
+                "host_api_value": e2e_host,
+                "host_api": "sgemv_run_group_host(q,k,v), sgemv_run_host(o), "
+                            "sgemv_run_group_host(gate,up), sgemv_run_host(down) (copies between "
+                            "the kernels), graph per packed copy"},
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
         "oracle_pack": oracle_pack,

@@ -214,6 +214,20 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
                     void* const* y_devs, int m, void* stream);
 
 /*
+ * The grouped run with x and the outputs in host memory, as sgemv_run_host
+ * is to sgemv_run: x_host (m x cols binary16) is copied to the first
+ * handle's staging buffer, the products run as in sgemv_run_group into each
+ * handle's own output staging, and y_i goes back to y_hosts[i] (m x rows_i
+ * binary16), all ordered on `stream`; the call returns without waiting, so
+ * the caller synchronises the stream before reading the outputs.  A handle
+ * may appear only once (SGEMV_ERR_ARG otherwise); calls that share a handle
+ * must be ordered on one stream.  Page-locked host buffers make the copies
+ * asynchronous.
+ */
+int sgemv_run_group_host(const sgemv_t* handles, int count, const void* x_host,
+                         void* const* y_hosts, int m, void* stream);
+
+/*
  * sgemv_run for 2 <= m <= min(64, max_m) that allocates nothing (the paper
  * has no counterpart: this is a deployment variant).  Meant for callers
  * that may not allocate device memory when they run the product: code under

@@ -10,9 +10,9 @@ package is a thin ctypes binding over it.
 from ._native import (SGEMV_ERR_ARG, SGEMV_ERR_CUDA, SGEMV_ERR_NONFINITE,
                       SGEMV_ERR_RANGE, SGEMV_ERR_STATE, SGEMV_ERR_TIMEOUT,
                       SGEMV_ERR_UNSUPPORTED, SGEMV_MAX_M, SGEMV_OK, SIGNATURES,
-                      SgemvError, SparseGemv, load, LIB_PATH, run_group)
+                      SgemvError, SparseGemv, load, LIB_PATH, run_group, run_group_host)
 
-__all__ = ["SparseGemv", "SgemvError", "load", "LIB_PATH", "SIGNATURES", "run_group",
+__all__ = ["SparseGemv", "SgemvError", "load", "LIB_PATH", "SIGNATURES", "run_group", "run_group_host",
            "SGEMV_OK", "SGEMV_ERR_ARG", "SGEMV_ERR_UNSUPPORTED",
            "SGEMV_ERR_CUDA", "SGEMV_ERR_STATE", "SGEMV_ERR_TIMEOUT",
            "SGEMV_ERR_NONFINITE", "SGEMV_ERR_RANGE", "SGEMV_MAX_M"]

@@ -41,6 +41,7 @@ SIGNATURES = {
     "sgemv_run": (_I, [_P, _P, _P, _I, _P]),
     "sgemv_run_host": (_I, [_P, _P, _P, _I, _P]),
     "sgemv_run_group": (_I, [_P, _I, _P, _P, _I, _P]),
+    "sgemv_run_group_host": (_I, [_P, _I, _P, _P, _I, _P]),
     "sgemv_run_noalloc": (_I, [_P, _P, _P, _I, _P]),
     "sgemv_status": (_I, [_P]),
     "sgemv_debug_withhold": (_I, [_P, _I]),
@@ -273,3 +274,20 @@ def run_group(mats, x, ys, stream=None) -> None:
     m = x.shape[0] if x.dim() == 2 else 1
     _check(load().sgemv_run_group(hs, n, x.data_ptr(), yp, m, _stream_ptr(stream)),
            "sgemv_run_group")
+
+
+def run_group_host(mats, x, ys, stream=None) -> None:
+    """run_group with host buffers: x (m x cols) and each ys[i] (m x rows_i)
+    are float16 numpy arrays or CPU tensors (ideally page-locked).
+    Asynchronous on `stream`: synchronise it before reading ys."""
+    n = len(mats)
+    if len(ys) != n:
+        raise ValueError("one output per matrix")
+
+    def ptr(a):
+        return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
+    hs = (ctypes.c_void_p * max(n, 1))(*[h.handle for h in mats])
+    yp = (ctypes.c_void_p * max(n, 1))(*[ptr(y) for y in ys])
+    m = x.shape[0] if len(x.shape) == 2 else 1
+    _check(load().sgemv_run_group_host(hs, n, ptr(x), yp, m, _stream_ptr(stream)),
+           "sgemv_run_group_host")

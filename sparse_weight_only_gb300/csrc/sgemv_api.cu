@@ -515,6 +515,9 @@ int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
   return SGEMV_OK;
 }
 
+static int run_group_checked(const sgemv_t* handles, int count, const void* x_dev,
+                             void* const* y_devs, int m, cudaStream_t s);
+
 int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
                     void* const* y_devs, int m, void* stream) {
   if (count < 0) return fail(SGEMV_ERR_ARG, "count=%d is negative", count);
@@ -553,7 +556,12 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
     return fail(SGEMV_ERR_ARG, "x_dev must be 16-byte aligned");
   DeviceGuard g(handles[0]->device);
   if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return run_group_checked(handles, count, x_dev, y_devs, m, static_cast<cudaStream_t>(stream));
+}
+
+// The grouped run after its arguments were checked, on the handles' device.
+static int run_group_checked(const sgemv_t* handles, int count, const void* x_dev,
+                             void* const* y_devs, int m, cudaStream_t s) {
   if (m == 0 || handles[0]->L.cols == 0) {
     for (int i = 0; i < count; ++i)
       if (int rc = run_checked(handles[i], x_dev, y_devs[i], m, s)) return rc;
@@ -708,6 +716,47 @@ int sgemv_run_group(const sgemv_t* handles, int count, const void* x_dev,
         k = 0;
       }
     }
+  }
+  return SGEMV_OK;
+}
+
+int sgemv_run_group_host(const sgemv_t* handles, int count, const void* x_host,
+                         void* const* y_hosts, int m, void* stream) {
+  if (count < 0) return fail(SGEMV_ERR_ARG, "count=%d is negative", count);
+  if (count == 0) return SGEMV_OK;
+  if (!handles || !y_hosts) return fail(SGEMV_ERR_ARG, "handles or y_hosts is NULL");
+  for (int i = 0; i < count; ++i) {
+    if (int rc = run_args_ok(handles[i], x_host, y_hosts[i], m)) return rc;
+    if (handles[i]->L.cols != handles[0]->L.cols)
+      return fail(SGEMV_ERR_ARG, "handle %d has cols=%d, handle 0 has cols=%d", i,
+                  handles[i]->L.cols, handles[0]->L.cols);
+    if (handles[i]->device != handles[0]->device)
+      return fail(SGEMV_ERR_ARG, "handles are on different devices");
+    for (int j = 0; j < i; ++j)
+      if (handles[j] == handles[i])
+        return fail(SGEMV_ERR_ARG, "handle %d appears twice (its output staging is shared)", i);
+  }
+  DeviceGuard g(handles[0]->device);
+  if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (m == 0) return SGEMV_OK;
+  // x into the first handle's staging buffer, the products into each
+  // handle's own, y back to the caller
+  const size_t xn = (size_t)m * handles[0]->L.cols * 2;
+  if (xn)
+    CUDA_TRY(cudaMemcpyAsync(handles[0]->d_xstage, x_host, xn, cudaMemcpyHostToDevice, s),
+             "copy x to device");
+  void* ys[64];
+  void** yd = count <= 64 ? ys : new void*[count];
+  for (int i = 0; i < count; ++i) yd[i] = handles[i]->d_ystage;
+  int rc = run_group_checked(handles, count, handles[0]->d_xstage, yd, m, s);
+  if (yd != ys) delete[] yd;
+  if (rc) return rc;
+  for (int i = 0; i < count; ++i) {
+    const size_t yn = (size_t)m * handles[i]->L.rows * 2;
+    if (yn)
+      CUDA_TRY(cudaMemcpyAsync(y_hosts[i], handles[i]->d_ystage, yn, cudaMemcpyDeviceToHost, s),
+               "copy y to host");
   }
   return SGEMV_OK;
 }

@@ -725,6 +725,9 @@ __global__ void __launch_bounds__(kNT, 1) k_m1_dual(const __grid_constant__ M1Du
 
 // Time of a 1:4 chunk against a 2:4 chunk in the M=1 kernel (a CTA-time
 // trace of the mixed q/k/v launch; 1.3 gave the shortest step of 1.0-1.5)
+#ifndef SGEMV_M1_PDL
+#define SGEMV_M1_PDL 1
+#endif
 #ifndef SGEMV_M1_COST14
 #define SGEMV_M1_COST14 1.3
 #endif
@@ -832,7 +835,7 @@ cudaError_t launch_pdl(Kernel kernel, const Params& p, int grid, size_t smem, cu
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = SGEMV_M1_PDL ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 

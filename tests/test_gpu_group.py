@@ -153,3 +153,27 @@ def test_group_rejects_overlapping_outputs(native, orc):
     buf = torch.empty((1, 96), dtype=torch.float16, device="cuda")
     with pytest.raises(native.SgemvError):
         native.run_group([h for h, _ in mats], x, [buf[:, :64], buf[:, 32:96]])
+
+
+@pytest.mark.parametrize("m", [1, 4, 33])
+def test_group_host_matches_device(native, orc, m):
+    """sgemv_run_group_host: x in, outputs out through host buffers, the same
+    products as sgemv_run_group on device buffers, bit for bit."""
+    cols = 1536
+    mats = _mats(native, orc, SPECS_MIXED[:6], cols, max_m=64)
+    hs = [h for h, _ in mats]
+    x = synth.activations(55 + m, m, cols)
+    ys = _ys(mats, m)
+    native.run_group(hs, torch.from_numpy(x).cuda(), ys)
+    torch.cuda.synchronize()
+    xh = torch.from_numpy(x).pin_memory()
+    yh = [torch.zeros((m, h.rows), dtype=torch.float16).pin_memory() for h in hs]
+    stream = torch.cuda.current_stream()
+    native.run_group_host(hs, xh, yh, stream)
+    stream.synchronize()
+    for (h, p), y, yy in zip(mats, ys, yh):
+        assert torch.equal(y.cpu(), yy), f"{h.rows} rows"
+        assert h.status() == 0
+    with pytest.raises(native.SgemvError) as e:          # a handle twice
+        native.run_group_host([hs[0], hs[0]], xh, [yh[0], yh[0]])
+    assert e.value.code == native.SGEMV_ERR_ARG
