@@ -335,6 +335,13 @@ constexpr int kRD = 32;                // "sub-stage done" barriers (ring)
 #define SGEMV_TC_ALIGN_PCT 50
 #endif
 constexpr int kAlignPct = SGEMV_TC_ALIGN_PCT;   // least share of the SMs a tile-aligned grid keeps
+#ifndef SGEMV_TC_DEC2
+#define SGEMV_TC_DEC2 1
+#endif
+// Decode warps take sub-stages in pairs: both decodes before both stores,
+// so that the two dependency chains interleave (1.5% off the config-4
+// verification step at M = 17..64).
+constexpr bool kDecodePairs = SGEMV_TC_DEC2 != 0;
 #ifndef SGEMV_TC_CLUSTER
 #define SGEMV_TC_CLUSTER 1
 #endif
@@ -531,7 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
     const int r = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     int uit = uit0, dtile = tile0;   // dtile: read by the checked build only
-    for (int s = 0; s < nsub; ++s) {
+    // sub-stage s of the weights -> A and metadata registers (false: a wait
+    // gave up)
+    auto decode_sub = [&](int s, uint32_t (&a0)[8], uint32_t (&a1)[8], uint32_t& m0,
+                          uint32_t& m1) -> bool {
       const int ui = s / SUBS, ls = s % SUBS;
       if (ls == 0 && ui > 0 && ++uit == U) {
         uit = 0;
@@ -539,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
       }
       const uint32_t wslot = wring + (uint32_t)((ui % kNW) * kStageW);
       if (ls == 0 && !__all_sync(0xffffffffu, wait(bar_wf + 8 * (ui % kNW), (uint32_t)((ui / kNW) & 1))))
-        break;
+        return false;
       const int scol0 = uit * UNIT_COLS + ls * 128;
       const int g0 = ((uit * UNIT_COLS) >> p.gshift) & ~3;
       int myG = (scol0 + 64 * h) >> p.gshift;
@@ -550,8 +560,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
         }
       }
       const uint32_t szw = lds32(wslot + kSzOff + (uint32_t)(r * 32 + (myG - g0) * 4));
-      uint32_t a0[8], a1[8];
-      uint32_t m0, m1;
       if constexpr (N == 2) {
         const int ch = 2 * ls + h;
         const uint4 v = lds128(wslot + kValsOff + (uint32_t)(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)));
@@ -596,11 +604,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_we + 8 * (ui % kNW));
       }
+      return true;
+    };
+    // ... -> tensor memory, once the A/metadata slot is free
+    auto store_sub = [&](int s, const uint32_t (&a0)[8], const uint32_t (&a1)[8], uint32_t m0,
+                         uint32_t m1) -> bool {
       // the A/metadata slot of s is free once the MMAs of s - NA are done
       const int t = s % NA;
       if (s >= NA && !__all_sync(0xffffffffu, wait(bar_dn + 8 * ((s - NA) % kRD),
                                                     (uint32_t)(((s - NA) / kRD) & 1))))
-        break;
+        return false;
       fence_after();
       const uint32_t slot_col = (uint32_t)(DCOLS + 32 * (4 * t + 2 * h));
       st8(tmem + lane_off + slot_col + 8, a0);
@@ -611,6 +624,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ TcPa
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_af + 8 * t);
+      return true;
+    };
+    if (kDecodePairs) {
+      // two sub-stages per pass: their decodes interleave, and the loop and
+      // waits are paid once per pair
+      for (int s = 0; s < nsub; s += 2) {
+        uint32_t a0[8], a1[8], b0[8], b1[8], m0, m1, n0, n1;
+        const bool two = s + 1 < nsub;
+        if (!decode_sub(s, a0, a1, m0, m1)) break;
+        if (two && !decode_sub(s + 1, b0, b1, n0, n1)) break;
+        if (!store_sub(s, a0, a1, m0, m1)) break;
+        if (two && !store_sub(s + 1, b0, b1, n0, n1)) break;
+      }
+    } else {
+      for (int s = 0; s < nsub; ++s) {
+        uint32_t a0[8], a1[8], m0, m1;
+        if (!decode_sub(s, a0, a1, m0, m1)) break;
+        if (!store_sub(s, a0, a1, m0, m1)) break;
+      }
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ======================= MMA issue ====================================
