@@ -73,6 +73,15 @@ def test_null_handle_calls(lib):
         assert rc == swo.SGEMV_ERR_ARG
     assert lib.sgemv_run(None, None, None, 1, None) == swo.SGEMV_ERR_ARG
     assert lib.sgemv_run_host(None, None, None, 1, None) == swo.SGEMV_ERR_ARG
+    # grouped runs: a negative count, NULL arrays, a NULL handle in the list
+    for name in ("sgemv_run_group", "sgemv_run_group_host"):
+        fn = getattr(lib, name)
+        assert fn(None, -1, None, None, 1, None) == swo.SGEMV_ERR_ARG
+        assert fn(None, 0, None, None, 1, None) == swo.SGEMV_OK       # count 0: no-op
+        assert fn(None, 2, None, None, 1, None) == swo.SGEMV_ERR_ARG
+        hs = (ctypes.c_void_p * 1)(None)
+        ys = (ctypes.c_void_p * 1)(None)
+        assert fn(hs, 1, None, ys, 1, None) == swo.SGEMV_ERR_ARG
     assert lib.sgemv_export(None, None, None, None, None) == swo.SGEMV_ERR_ARG
     assert lib.sgemv_import(None, None, None, None, None) == swo.SGEMV_ERR_ARG
     assert lib.sgemv_create(None, 1, 64, 2, 64, 1, 0) == swo.SGEMV_ERR_ARG
