@@ -486,9 +486,11 @@ __device__ __forceinline__ void stream_prologue(RowProducer<N, MODE>& prod, cons
   int k = 0;
 #pragma unroll
   for (int t = 0; t < kS; ++t) {
-    if (t > 0 && k == 0) prod.advance(p, c0, lane, nrw);
-    if (nrw > 0 && prod.pr < nrw)
-      prod.issue_rt(k, ring16 + t * kStage, ring8 + t * kStage, k < ipr - 1 || last_on);
+    if (nrw > 0) {   // (a warp without rows never starts its producer)
+      if (t > 0 && k == 0) prod.advance(p, c0, lane, nrw);
+      if (prod.pr < nrw)
+        prod.issue_rt(k, ring16 + t * kStage, ring8 + t * kStage, k < ipr - 1 || last_on);
+    }
     cp_commit();
     k = k + 1 == ipr ? 0 : k + 1;
   }
