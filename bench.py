@@ -521,7 +521,7 @@ def run_ours(args, rank, world, local):
                   flush=True)
         return 0
 
-    # the survey's protocol as well: a graph of >= 200 back-to-back launches
+    # the per-call protocol as well: a graph of >= 200 back-to-back launches
     # (whole steps, rotating copies), median of 10 timed replays
     n200 = max(block, -(-200 // per_step))
     g200 = capture(n200, 0)
