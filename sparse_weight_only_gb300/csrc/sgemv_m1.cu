@@ -541,15 +541,82 @@ __device__ __forceinline__ void row_group(SliceCtx<N, MODE>& c, int r0, int warp
   }
 }
 
+// A row's total (CTA row lr of matrix seg) into y, or into the partial
+// carried over K slices.
+__device__ __forceinline__ void store_row(const M1Params& p, int seg, int r0, int lr, int sl,
+                                          float* part, float v) {
+  const M1Seg& sg = p.seg[seg];
+  __half* yrow = sg.y + (r0 + lr - sg.row_begin);
+  if (p.nslices == 1) {
+    *yrow = __float2half_rn(v);
+  } else {
+    const float t = (sl ? part[lr] : 0.0f) + v;
+    if (sl == p.nslices - 1)
+      *yrow = __float2half_rn(t);
+    else
+      part[lr] = t;
+  }
+}
+
+// Rows of one item (IPR = 1), two at a time: one exchange across the
+// half-warps leaves row j's partials in lanes 0..15 and row j + 1's in lanes
+// 16..31, and four more butterfly steps finish both (the same additions,
+// pair for pair, as a butterfly over each row alone).
+template <int N, int MODE>
+__device__ __forceinline__ void stream_rows_paired(SliceCtx<N, MODE>& c, int r0, int warp,
+                                                   int sl, float* part) {
+  const M1Params& p = *c.p;
+  const bool hi = (c.lane & 16) != 0;
+  int seg = 0;
+  auto row_acc = [&](int j) -> float {
+    const int row = r0 + warp + kNW * j;
+    seg = seg_from<MODE>(p, seg, row);
+    const M1Seg& sg = p.seg[seg];
+    const bool g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
+    float acc = 0.0f;
+    row_items<N, MODE, 1, -1, 0>(c, g64, acc);
+    c.par ^= kStage;
+    return acc;
+  };
+  for (int j = 0; j < c.nrw; j += 2) {
+    const float a0 = row_acc(j);
+    const int seg0 = seg;
+    if (j + 1 < c.nrw) {
+      const float a1 = row_acc(j + 1);
+      float v = (hi ? a1 : a0) + __shfl_xor_sync(0xffffffffu, hi ? a0 : a1, 16);
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if ((c.lane & 15) == 0)
+        store_row(p, hi ? seg : seg0, r0, warp + kNW * (j + (hi ? 1 : 0)), sl, part, v);
+    } else {
+      float v = a0;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (c.lane == 0) store_row(p, seg0, r0, warp + kNW * j, sl, part, v);
+    }
+  }
+}
+
+#ifndef SGEMV_M1_PAIR1
+#define SGEMV_M1_PAIR1 1
+#endif
+
 // The warp's rows of one K slice, IPR items each.
 template <int N, int MODE, int IPR>
 __device__ __forceinline__ void stream_slice(SliceCtx<N, MODE>& c, int r0, int warp, int sl,
                                              float* part) {
   constexpr bool kStatic = kStaticStages == 1 ? (IPR % kS == 0 || kS % IPR == 0)
                                                : kStaticStages == 2 && IPR % kS == 0;
-  constexpr int RU = kStatic && IPR < kS ? kS / IPR : 1;
-  int seg = 0;
-  for (int j = 0; j < c.nrw; j += RU) row_group<N, MODE, IPR, RU, 0>(c, r0, warp, j, sl, part, seg);
+  if constexpr (IPR == 1 && !kStatic && SGEMV_M1_PAIR1 && MODE != kMany) {
+    // a one-item row is short: reducing two rows together saves a fifth of
+    // the reduction per row (single-matrix launches only: in the grouped
+    // kernels the larger body cost more than it saved)
+    stream_rows_paired<N, MODE>(c, r0, warp, sl, part);
+  } else {
+    constexpr int RU = kStatic && IPR < kS ? kS / IPR : 1;
+    int seg = 0;
+    for (int j = 0; j < c.nrw; j += RU) row_group<N, MODE, IPR, RU, 0>(c, r0, warp, j, sl, part, seg);
+  }
 }
 
 // Items per row the kernel is compiled for: 2:4 slices of up to 128
