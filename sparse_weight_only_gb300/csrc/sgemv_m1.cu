@@ -45,8 +45,9 @@ namespace {
 #ifndef SGEMV_M1_NT
 #define SGEMV_M1_NT 512
 #endif
-constexpr int kNT = SGEMV_M1_NT;    // threads per CTA (one CTA per SM)
-constexpr int kNW = kNT / 32;
+#ifndef SGEMV_M1_NT_MANY
+#define SGEMV_M1_NT_MANY 640
+#endif
 #ifndef SGEMV_M1_D
 #define SGEMV_M1_D 2
 #endif
@@ -296,16 +297,26 @@ __device__ __forceinline__ float chunk_dot(const uint4& v, const uint2& ix,
   }
 }
 
-// Rows of a CTA interleave over its warps: the warp's j-th row is local row
-// warp + kNW j.
-__device__ __forceinline__ int warp_nrows(int warp, int nr) {
-  return warp < nr ? (nr - warp + kNW - 1) / kNW : 0;
-}
-
 // MODE of a launch: kOne = one matrix, groups of 64 columns not split
 // across chunks; kOneG64 = one 1:4 matrix with 64-column groups (two groups
 // per chunk); kMany = several matrices, the split decided per row.
 constexpr int kOne = 0, kOneG64 = 1, kMany = 2;
+
+// Threads per CTA (one CTA per SM) of a launch mode: 20 warps for the
+// grouped launches, 16 for one matrix (each measured the faster there; at
+// 640 threads the kernel fits in under 100 registers without spilling).
+template <int MODE>
+constexpr int kNTm = MODE == kMany ? SGEMV_M1_NT_MANY : SGEMV_M1_NT;
+template <int MODE>
+constexpr int kNWm = kNTm<MODE> / 32;
+
+// Rows of a CTA interleave over its warps: the warp's j-th row is local row
+// warp + kNW j.
+template <int MODE>
+__device__ __forceinline__ int warp_nrows(int warp, int nr) {
+  constexpr int kNW = kNWm<MODE>;
+  return warp < nr ? (nr - warp + kNW - 1) / kNW : 0;
+}
 
 // Matrix of launch row `row`, searched forward from `seg` (a warp visits its
 // rows in increasing order within a K slice).
@@ -345,8 +356,8 @@ struct RowProducer {
     sp = sg.sz + (size_t)lr * sg.gstride + ((ch * C::CPC) >> sg.gshift);
     sstep = (32 * C::CPC) >> sg.gshift;
     g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
-    vstep = kNW * p.cstride;
-    sstep_row = kNW * sg.gstride;
+    vstep = kNWm<MODE> * p.cstride;
+    sstep_row = kNWm<MODE> * sg.gstride;
     next_begin = MODE == kMany && seg + 1 < p.nseg ? p.seg[seg + 1].row_begin : 0x7fffffff;
   }
   __device__ __forceinline__ void start(const M1Params& p, int r0, int warp, int c0, int lane) {
@@ -358,7 +369,7 @@ struct RowProducer {
   // to the warp's next row (pointers only while it has one)
   __device__ __forceinline__ void advance(const M1Params& p, int c0, int lane, int nrw) {
     ++pr;
-    row += kNW;
+    row += kNWm<MODE>;
     if (pr >= nrw) return;
     if (row < next_begin) {
       vp += vstep;
@@ -502,7 +513,7 @@ template <int N, int MODE, int IPR, int SO0>
 __device__ __forceinline__ void one_row(SliceCtx<N, MODE>& c, int r0, int warp, int j, int sl,
                                         float* part, int& seg) {
   const M1Params& p = *c.p;
-  const int lr = warp + kNW * j;
+  const int lr = warp + kNWm<MODE> * j;
   const int row = r0 + lr;
   seg = seg_from<MODE>(p, seg, row);
   const M1Seg& sg = p.seg[seg];
@@ -569,7 +580,7 @@ __device__ __forceinline__ void stream_rows_paired(SliceCtx<N, MODE>& c, int r0,
   const bool hi = (c.lane & 16) != 0;
   int seg = 0;
   auto row_acc = [&](int j) -> float {
-    const int row = r0 + warp + kNW * j;
+    const int row = r0 + warp + kNWm<MODE> * j;
     seg = seg_from<MODE>(p, seg, row);
     const M1Seg& sg = p.seg[seg];
     const bool g64 = N == 1 && (MODE == kMany ? sg.g64 != 0 : MODE == kOneG64);
@@ -587,12 +598,12 @@ __device__ __forceinline__ void stream_rows_paired(SliceCtx<N, MODE>& c, int r0,
 #pragma unroll
       for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
       if ((c.lane & 15) == 0)
-        store_row(p, hi ? seg : seg0, r0, warp + kNW * (j + (hi ? 1 : 0)), sl, part, v);
+        store_row(p, hi ? seg : seg0, r0, warp + kNWm<MODE> * (j + (hi ? 1 : 0)), sl, part, v);
     } else {
       float v = a0;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (c.lane == 0) store_row(p, seg0, r0, warp + kNW * j, sl, part, v);
+      if (c.lane == 0) store_row(p, seg0, r0, warp + kNWm<MODE> * j, sl, part, v);
     }
   }
 }
@@ -652,7 +663,7 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
 
   const int r0 = cta * p.rows_per_cta;
   const int nr = max(0, min(p.rows, r0 + p.rows_per_cta) - r0);
-  const int nrw = warp_nrows(warp, nr);
+  const int nrw = warp_nrows<MODE>(warp, nr);
 
   // The ring starts zeroed: a lane past a ragged slice reads a stage it did
   // not fill, and must find codes in range there (its table slots are zero).
@@ -710,7 +721,7 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
     {
       const int ncols = nch * C::CPC;
       const int col0 = c0 * C::CPC;
-      for (int t = threadIdx.x; t < ncols / 8; t += kNT) {
+      for (int t = threadIdx.x; t < ncols / 8; t += kNTm<MODE>) {
         const int col = col0 + 8 * t;
         uint4 q = make_uint4(0, 0, 0, 0);
         if (col < p.cols) q = *reinterpret_cast<const uint4*>(p.x + col);
@@ -727,7 +738,7 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
     {
       const int l = threadIdx.x & 31;
       const uint32_t colbase = smem_s + (uint32_t)((l >> 4) * S) * 128u + (l & 15) * 8u;
-      for (int u_it = warp; u_it < ipr * kUnitsPerChunk; u_it += kNW) {
+      for (int u_it = warp; u_it < ipr * kUnitsPerChunk; u_it += kNWm<MODE>) {
         const int i = u_it / kUnitsPerChunk, u = u_it % kUnitsPerChunk;
         const int cl = l + 32 * i;
         float xv[C::UC];
@@ -774,7 +785,7 @@ __device__ __forceinline__ void m1_body(const M1Params& p, int cta) {
 }
 
 template <int N, int MODE>
-__global__ void __launch_bounds__(kNT, 1) k_m1(const __grid_constant__ M1Params p) {
+__global__ void __launch_bounds__(kNTm<MODE>, 1) k_m1(const __grid_constant__ M1Params p) {
   m1_body<N, MODE>(p, blockIdx.x);
 }
 
@@ -785,7 +796,7 @@ struct M1DualParams {
   int grid_a;
 };
 
-__global__ void __launch_bounds__(kNT, 1) k_m1_dual(const __grid_constant__ M1DualParams p) {
+__global__ void __launch_bounds__(kNTm<kMany>, 1) k_m1_dual(const __grid_constant__ M1DualParams p) {
   if ((int)blockIdx.x < p.grid_a)
     m1_body<2, kMany>(p.a, blockIdx.x);
   else
@@ -837,7 +848,7 @@ cudaError_t plan_m1(const Layout* Ls, const RunArgs* as, int count, int ctas, M1
   if (total_rows == 0) return cudaSuccess;
   if (total_rows >= (1ll << 31)) return cudaErrorNotSupported;
   if (ctas <= 0) return cudaErrorNotSupported;
-  const size_t ring = (size_t)kNW * kS * kStage;
+  const size_t ring = (size_t)kNWm<MODE> * kS * kStage;
   const size_t part_max = 4096;   // rows_per_cta <= 1024 when K is sliced
   const size_t room = kSmemLimit - kTabAlign - ring - part_max;
   const int max_cpl = min((int)(room / (C::TAB_PER_CPL + C::X_PER_CPL)), max_ipr<N>());
@@ -885,8 +896,8 @@ cudaError_t plan_m1(const Layout* Ls, const RunArgs* as, int count, int ctas, M1
 }
 
 template <typename Kernel, typename Params>
-cudaError_t launch_pdl(Kernel kernel, const Params& p, int grid, size_t smem, cudaStream_t s,
-                       bool (&attr_set)[64]) {
+cudaError_t launch_pdl(Kernel kernel, const Params& p, int grid, int threads, size_t smem,
+                       cudaStream_t s, bool (&attr_set)[64]) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
@@ -897,7 +908,7 @@ cudaError_t launch_pdl(Kernel kernel, const Params& p, int grid, size_t smem, cu
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kNT);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -917,7 +928,7 @@ cudaError_t launch_m1_n(const Layout* Ls, const RunArgs* as, int count, cudaStre
   cudaError_t e = plan_m1<N, MODE>(Ls, as, count, num_sms(), p, grid, smem);
   if (e != cudaSuccess || grid == 0) return e;
   static bool attr_set[64] = {false};
-  return launch_pdl(k_m1<N, MODE>, p, grid, smem, s, attr_set);
+  return launch_pdl(k_m1<N, MODE>, p, grid, kNTm<MODE>, smem, s, attr_set);
 }
 
 }  // namespace
@@ -969,7 +980,7 @@ cudaError_t launch_m1_group_dual(const Layout* L2, const RunArgs* a2, int n2, co
   if (g2 == 0 || g1 == 0) return cudaErrorNotSupported;
   p.grid_a = g2;
   static bool attr_set[64] = {false};
-  return launch_pdl(k_m1_dual, p, g2 + g1, s2 > s1 ? s2 : s1, s, attr_set);
+  return launch_pdl(k_m1_dual, p, g2 + g1, kNTm<kMany>, s2 > s1 ? s2 : s1, s, attr_set);
 }
 
 int max_group() { return kMaxSeg; }
