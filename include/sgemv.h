@@ -267,13 +267,15 @@ int sgemv_status(sgemv_t h);
 
 /*
  * Failure-detection test hook (not a paper operation).  The next `runs`
- * batch products on this handle (2 <= m <= 64) make their bounded wait run
- * out: for 2 <= m <= 16 every cluster rank withholds its split-K partial
- * sums, for larger m the kernel withholds its x copies, and the wait limit
- * drops to about 20 microseconds.  sgemv_status then returns
- * SGEMV_ERR_TIMEOUT and y of those calls is undefined.  Nothing the kernel
- * waits for is in flight when it gives up, the device stays usable and
- * later calls run normally.  m = 1 calls do not consume the hook.
+ * batch products on this handle with 2 <= m <= 8 or 17 <= m <= 64 make
+ * their bounded wait run out: for 2 <= m <= 8 every cluster rank withholds
+ * its split-K partial sums, for m >= 17 the kernel withholds its x copies,
+ * and the wait limit drops to about 20 microseconds.  sgemv_status then
+ * returns SGEMV_ERR_TIMEOUT and y of those calls is undefined.  Nothing the
+ * kernel waits for is in flight when it gives up, the device stays usable
+ * and later calls run normally.  Calls with m = 1 or 9 <= m <= 16 (whose
+ * kernels wait on no copy, only on cluster barriers) do not consume the
+ * hook.
  * runs = 0 cancels; runs < 0 -> SGEMV_ERR_ARG.
  */
 int sgemv_debug_withhold(sgemv_t h, int runs);

@@ -32,7 +32,7 @@
 //    into a temporary that is scaled by s and added in fp32.
 //  * split-K across the CTAs of a thread-block cluster, reduced through
 //    distributed shared memory in rank order -- deterministic, no global
-//    scratch.  Up to two n-tiles (m <= 16) every CTA pushes its partial rows
+//    scratch.  With one n-tile (m <= 8) every CTA pushes its partial rows
 //    to their owner rank with remote stores counted on the owner's mbarrier
 //    (one split cluster barrier, arrive at launch and wait after the main
 //    loop, orders the setup); wider tiles are written to each CTA's shared
@@ -206,10 +206,14 @@ constexpr unsigned long long kInjectWaitNs = 20000ull;
 
 // The split-K partials travel by remote stores from the accumulators (one
 // 8-byte store per row pair and n-tile, counted on the owner's mbarrier) for
-// up to two n-tiles; wider tiles write them to shared memory and the owners
-// pull them after a cluster barrier, which costs less than thousands of small
-// remote stores per CTA.
-__host__ __device__ constexpr bool push_reduce(int nt) { return nt <= 2; }
+// one n-tile; wider tiles write them to shared memory and the owners pull
+// them after a cluster barrier.  At two n-tiles the pulled form measured
+// 1-3 us faster per layer step (the pushed one issues 1024 remote stores per
+// CTA); at one n-tile the two forms time the same.
+#ifndef SGEMV_MMA_PUSH_NT
+#define SGEMV_MMA_PUSH_NT 1
+#endif
+__host__ __device__ constexpr bool push_reduce(int nt) { return nt <= SGEMV_MMA_PUSH_NT; }
 
 // Rows of the CTA tile that cluster rank q reduces: [q R / n, (q + 1) R / n).
 __device__ __forceinline__ int owner_rank(int r, int nsplit) {
@@ -719,9 +723,11 @@ int g_sms[64] = {0};
 }  // namespace
 
 bool withhold_applies(const Layout& L, int m) {
-  // m <= 16: this kernel's pushed split-K sums; larger m: the tcgen05
-  // kernel's x copies
-  return m >= 2 && L.rows > 0 && L.cols > 0;
+  // one n-tile: this kernel's pushed split-K sums; m > 16: the tcgen05
+  // kernel's x copies.  The pulled sums of wider tiles wait on cluster
+  // barriers only, which every rank reaches: nothing to withhold there.
+  const bool pushed = push_reduce((m + 7) / 8);
+  return m >= 2 && (pushed || m > 16) && L.rows > 0 && L.cols > 0;
 }
 
 cudaError_t launch_mma_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s) {
