@@ -255,12 +255,13 @@ int sgemv_run_noalloc(sgemv_t h, const void* x_dev, void* y_dev, int m, void* st
  * word (SGEMV_OK if no kernel reported an error since the last call).  A
  * batch kernel reports SGEMV_ERR_TIMEOUT when one of its bounded waits gave
  * up after about a second; the outputs of that call are then undefined and
- * later calls are unaffected.  2 <= m <= 16: the split-K reduction waiting
+ * later calls are unaffected.  2 <= m <= 8: the split-K reduction waiting
  * for the partial sums of the other CTAs of its cluster -- every CTA still
  * issues all of its sends and no CTA retires before every CTA of its cluster
  * has issued them, so no late store lands in a retired CTA; what the limit
  * cannot guard against is a CTA that never reaches its sends (the launch
- * then does not finish).  17 <= m <= 64: the waits for its own TMA copies
+ * then does not finish).  9 <= m <= 16 reduce between cluster barriers that
+ * every CTA reaches, with no such wait.  17 <= m <= 64: the waits for its own TMA copies
  * and MMAs -- it then stops issuing work, lets the copies it issued land,
  * frees its tensor memory and completes its split-K counters. */
 int sgemv_status(sgemv_t h);
