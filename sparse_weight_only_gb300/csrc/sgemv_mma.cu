@@ -24,10 +24,10 @@
 //    reads are conflict-free), one ldmatrix.x4 per n-tile and k-tile.
 //  * weights and x: the CTA's 128 rows x K sub-slice (codes, positions and
 //    the sub-slice's scale/zero words) and the sub-slice's x columns are
-//    copied into shared memory with cp.async, double-buffered across
-//    sub-slices; the first sub-slice's weights are in flight before the
-//    wait for the previous kernel.  Warps read their rows from padded rows of
-//    the buffer (conflict-free).
+//    copied into shared memory with cp.async, double-buffered across equal
+//    sub-slices, as few as fit; the first sub-slice's weights are in flight
+//    before the wait for the previous kernel.  Warps read their rows from
+//    padded rows of the buffer (conflict-free).
 //  * scale: each k-tile lies inside one group; the MMA accumulates a group
 //    into a temporary that is scaled by s and added in fp32.
 //  * split-K across the CTAs of a thread-block cluster, reduced through
@@ -56,6 +56,19 @@ constexpr int kRowsCta = 16 * kW;     // weight rows per CTA
 constexpr int kMaxSplit = SGEMV_MMA_MAXSPLIT;  // CTAs per cluster (portable limit 8)
 constexpr size_t kSmemPerCta = 113 * 1024;  // two CTAs per SM
 constexpr int kCtasPerSm = 2;
+// Shared-memory buffers (weights + x) of the sub-slice ring.  Two: three or
+// four, with as many smaller sub-slices, measured 2-11 us slower per layer
+// step at m = 4..16.
+#ifndef SGEMV_MMA_STAGES
+#define SGEMV_MMA_STAGES 2
+#endif
+constexpr int kStages = SGEMV_MMA_STAGES;
+static_assert(kStages >= 2 && kStages <= 6, "sub-slice ring: 2..6 buffers");
+// Sub-slices per CTA the planner aims for (at least; smaller ones when the
+// shared memory needs it)
+#ifndef SGEMV_MMA_NSUB_MIN
+#define SGEMV_MMA_NSUB_MIN 1
+#endif
 #ifndef SGEMV_MMA_PDL
 #define SGEMV_MMA_PDL 1
 #endif
@@ -325,17 +338,17 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(const __grid_constant__ Mm
   const int mp = NT * 8;                       // padded activation rows
   const int xs_stride = p.sub_chunks * CPC + 8; // halves per staged x row
   const WGeom W(p.sub_chunks, p.sub_groups);
-  // shared memory: x of two sub-slices | two weight buffers | (pushed
-  // reduction) the receive buffer, one slot of ceil(R / nsplit) rows x mp
-  // per rank, and its mbarrier.  Sub-slice s uses x and weight buffer s & 1.
-  // The pulled reduction writes its partial tile over the front once the
-  // main loop is done.
+  // shared memory: x of kStages sub-slices | kStages weight buffers |
+  // (pushed reduction) the receive buffer, one slot of ceil(R / nsplit) rows
+  // x mp per rank, and its mbarrier.  Sub-slice s uses x and weight buffer
+  // s % kStages.  The pulled reduction writes its partial tile over the
+  // front once the main loop is done.
   const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(smem);
   const int xs_bytes = (mp * xs_stride * 2 + 127) & ~127;
-  const uint32_t wbuf0 = xs_s + (uint32_t)(2 * xs_bytes);
+  const uint32_t wbuf0 = xs_s + (uint32_t)(kStages * xs_bytes);
   float* part = reinterpret_cast<float*>(smem);
   const int rq = (kRowsCta + p.nsplit - 1) / p.nsplit;
-  const uint32_t recv_s = wbuf0 + (uint32_t)(2 * W.bytes);
+  const uint32_t recv_s = wbuf0 + (uint32_t)(kStages * W.bytes);
   const uint32_t rbar = recv_s + (uint32_t)(p.nsplit * rq * mp * 4);
   const float* recv = reinterpret_cast<const float*>(smem + (recv_s - xs_s));
 
@@ -405,37 +418,50 @@ __global__ void __launch_bounds__(kW * 32, 2) k_mma24(const __grid_constant__ Mm
                      in ? p.x + (size_t)w.r * p.cols + col : p.x, in ? 16 : 0);
     }
   };
-  // weights of the first sub-slice: in flight while the previous kernel ends
-  if (nsub > 0) {
-    const int ce = min(c_end, c_begin + p.sub_chunks);
-    stage_weights(p, W, wbuf0, row0, c_begin, ce, (c_begin * CPC) >> p.gshift,
+  // weights of the first kStages - 1 sub-slices: in flight while the
+  // previous kernel ends (one commit group)
+  for (int sp = 0; sp < kStages - 1 && sp < nsub; ++sp) {
+    const int cs = c_begin + sp * p.sub_chunks, ce = min(c_end, cs + p.sub_chunks);
+    stage_weights(p, W, wbuf0 + (uint32_t)(sp * W.bytes), row0, cs, ce, (cs * CPC) >> p.gshift,
                   min(p.ngroups - 1, (ce * CPC - 1) >> p.gshift));
   }
   cp_commit();
-  // x may be written by the previous kernel: wait for it only now
+  // x may be written by the previous kernel: wait for it only now; one
+  // commit group per sub-slice's x
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  if (nsub > 0) stage_x(xs_s, c_begin, min(c_end, c_begin + p.sub_chunks));
-  cp_commit();
+  for (int sp = 0; sp < kStages - 1; ++sp) {
+    if (sp < nsub) {
+      const int cs = c_begin + sp * p.sub_chunks;
+      stage_x(xs_s + (uint32_t)(sp * xs_bytes), cs, min(c_end, cs + p.sub_chunks));
+    }
+    cp_commit();
+  }
 
+  // Ring of kStages buffers: sub-slice i sits in buffer i % kStages; while
+  // one is computed the next kStages - 1 are in flight.  Every iteration
+  // commits one group, so "sub-slice sidx landed" is always "at most
+  // kStages - 1 groups pending".
   for (int sidx = 0; sidx < nsub; ++sidx) {
     const int cs = c_begin + sidx * p.sub_chunks;
     const int ce = min(c_end, cs + p.sub_chunks);
     const int g0 = (cs * CPC) >> p.gshift;
-    const uint32_t wb = wbuf0 + (uint32_t)((sidx & 1) * W.bytes);
-    const uint32_t ld_x = ld_base + (uint32_t)((sidx & 1) * xs_bytes);
-    __syncthreads();  // previous sub-slice fully consumed: the other buffers are free
-    if (sidx + 1 < nsub) {
-      // the next sub-slice's weights and x, in flight during this one
-      const int ns = ce, ne = min(c_end, ns + p.sub_chunks);
-      const int nb = (sidx + 1) & 1;
+    const int bi = sidx % kStages;
+    const uint32_t wb = wbuf0 + (uint32_t)(bi * W.bytes);
+    const uint32_t ld_x = ld_base + (uint32_t)(bi * xs_bytes);
+    __syncthreads();  // previous sub-slice fully consumed: its buffers are free
+    if (sidx + kStages - 1 < nsub) {
+      // sub-slice sidx + kStages - 1 into the buffers sub-slice sidx - 1 used
+      const int ns = c_begin + (sidx + kStages - 1) * p.sub_chunks;
+      const int ne = min(c_end, ns + p.sub_chunks);
+      const int nb = (sidx + kStages - 1) % kStages;
       stage_weights(p, W, wbuf0 + (uint32_t)(nb * W.bytes), row0, ns, ne,
                     (ns * CPC) >> p.gshift, min(p.ngroups - 1, (ne * CPC - 1) >> p.gshift));
       stage_x(xs_s + (uint32_t)(nb * xs_bytes), ns, ne);
     }
     cp_commit();
-    cp_wait<1>();     // this thread's copies of sub-slice sidx landed
-    __syncthreads();  // ... and every thread's
+    cp_wait<kStages - 1>();   // this thread's copies of sub-slice sidx landed
+    __syncthreads();          // ... and every thread's
     for (int c = cs; c < ce; ++c) {
       const int cc = c - cs;
       uint4 v_g = make_uint4(0, 0, 0, 0), v_g8 = v_g;
@@ -629,7 +655,7 @@ size_t mma_smem(int nt, int sc, int group, int cpc, int nsplit) {
   const int mp = nt * 8;
   const WGeom W(sc, (sc * cpc + group - 1) / group + 1);
   const size_t xs = ((size_t)mp * (sc * cpc + 8) * 2 + 127) & ~(size_t)127;
-  const size_t main = 2 * xs + 2 * (size_t)W.bytes;
+  const size_t main = (size_t)kStages * (xs + (size_t)W.bytes);
   if (!push_reduce(nt)) {
     const size_t red = (size_t)kRowsCta * mp * 4;
     return main > red ? main : red;
@@ -670,10 +696,15 @@ cudaError_t launch_nt(const Layout* Ls, const RunArgs* as, int count, cudaStream
   nsplit = max(1, min(kMaxSplit, min(nsplit, chunks)));
   const int split_chunks = (chunks + nsplit - 1) / nsplit;
   nsplit = (chunks + split_chunks - 1) / split_chunks;
-  // sub-slices: as many chunks as fit two CTAs per SM (the smallest group
-  // has the most scale/zero words per sub-slice)
-  int sub = min(split_chunks, 64);
-  while (sub > 1 && mma_smem(NT, sub, gmin, CPC, nsplit) > kSmemPerCta) sub = (sub + 1) / 2;
+  // sub-slices of equal size, as few as fit two CTAs per SM (the smallest
+  // group has the most scale/zero words per sub-slice); each costs two CTA
+  // barriers and a pipeline fill, and more, smaller ones measured slower
+  int nsb = max(1, min(SGEMV_MMA_NSUB_MIN, split_chunks));
+  int sub = min(64, (split_chunks + nsb - 1) / nsb);
+  while (sub > 1 && mma_smem(NT, sub, gmin, CPC, nsplit) > kSmemPerCta) {
+    ++nsb;
+    sub = (split_chunks + nsb - 1) / nsb;
+  }
   const size_t smem = mma_smem(NT, sub, gmin, CPC, nsplit);
   if (smem > 227 * 1024) return cudaErrorNotSupported;
   p.x = a.x;
