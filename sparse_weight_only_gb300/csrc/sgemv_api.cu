@@ -451,9 +451,9 @@ static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s)
     CUDA_TRY(cudaMemsetAsync(a.y, 0, (size_t)m * L.rows * sizeof(__half), s), "zero y");
     return SGEMV_OK;
   }
-  // m = 1: the CUDA-core pair-table kernel; 2 <= m <= 16: the warp-level
-  // sparse MMA kernel; 17 <= m <= 64: the tcgen05 kernel (each measured the
-  // fastest in its range on the verification-batch layer set)
+  // m = 1: the CUDA-core pair-table kernel; 2 <= m <= kMmaSyncMaxM (24):
+  // the warp-level sparse MMA kernel; up to 64: the tcgen05 kernel (each
+  // measured the fastest in its range on the verification-batch layer set)
   cudaError_t e = m == 1                       ? sgemv::launch_m1(L, a, s)
                   : m <= sgemv::kMmaSyncMaxM ? sgemv::launch_mma(L, a, s)
                                              : sgemv::launch_tc(L, a, h->tc, s);
@@ -614,7 +614,7 @@ static int run_group_checked(const sgemv_t* handles, int count, const void* x_de
         }
       return SGEMV_OK;
     }
-    // 2 <= m <= 16: one launch of the sparse MMA kernel per N and per
+    // 2 <= m <= kMmaSyncMaxM: one launch of the sparse MMA kernel per N and per
     // max_group() matrices
     const int cap = sgemv::max_group();
     for (int n = 1; n <= 2; ++n) {

@@ -177,7 +177,12 @@ int report_cuda(cudaError_t e, const char* what);
 // waits that the failure-detection hook can make run out.
 bool withhold_applies(const Layout& L, int m);
 // Largest m that the warp-level sparse MMA kernel (sgemv_mma.cu) takes;
-// larger batches run the tcgen05 kernel (sgemv_tc.cu).
-constexpr int kMmaSyncMaxM = 16;
+// larger batches run the tcgen05 kernel (sgemv_tc.cu).  Up to three n-tiles
+// the mma.sp kernel measured faster (layer steps at m = 17 / 24: 74-77 us
+// against 86 us); at four (m = 25..32) the tcgen05 kernel is.
+#ifndef SGEMV_MMA_MAX_M
+#define SGEMV_MMA_MAX_M 24
+#endif
+constexpr int kMmaSyncMaxM = SGEMV_MMA_MAX_M;
 
 }  // namespace sgemv
