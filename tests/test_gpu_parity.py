@@ -168,6 +168,24 @@ def test_run_parity_more_tiles_than_ctas(native, orc, n_keep, m):
             f"{rows}x{cols} {n_keep}:4 m={m}")
 
 
+@pytest.mark.parametrize("n_keep,m", [(2, 4), (2, 20), (1, 12)])
+def test_mma_unsplit_tiles(native, orc, n_keep, m):
+    """The mma.sp batch kernel when the row tiles alone fill the GPU: 20000
+    rows are 157 tiles of 128, more than one wave of two CTAs per SM can
+    split, so every cluster is a single CTA that walks the whole of K and
+    reduces with itself (pushed sums at one n-tile, pulled at two or
+    three)."""
+    rows, cols, group = 20000, 1024, 64
+    W = synth.weight_outliers(rows + 7 * m + n_keep, rows, cols)
+    p = orc.pack(W, n_keep, group)
+    h = native.SparseGemv(rows, cols, n_keep, group, max_m=m)
+    h.import_canonical(p.vals, p.idx, p.scale, p.zero)
+    x = synth.activations(m + 11, m, cols)
+    y = _run(h, x)
+    check_y(orc, y, orc.matvec(p, x), np.abs(orc.dequant(p)).sum(axis=1),
+            f"{rows}x{cols} {n_keep}:4 m={m}")
+
+
 def test_run_host_matches_device(native, orc):
     rows, cols, n_keep, group = 130, 1024, 2, 64
     W = _weight(99, rows, cols, "outliers")
