@@ -54,8 +54,11 @@ constexpr int kRowsCta = 16 * kW;     // weight rows per CTA
 #define SGEMV_MMA_MAXSPLIT 8
 #endif
 constexpr int kMaxSplit = SGEMV_MMA_MAXSPLIT;  // CTAs per cluster (portable limit 8)
-constexpr size_t kSmemPerCta = 113 * 1024;  // two CTAs per SM
-constexpr int kCtasPerSm = 2;
+#ifndef SGEMV_MMA_CPS
+#define SGEMV_MMA_CPS 2
+#endif
+constexpr int kCtasPerSm = SGEMV_MMA_CPS;   // CTAs resident per SM
+constexpr size_t kSmemPerCta = (kCtasPerSm == 1 ? 227 : 113) * 1024;
 // Shared-memory buffers (weights + x) of the sub-slice ring.  Two: three or
 // four, with as many smaller sub-slices, measured 2-11 us slower per layer
 // step at m = 4..16.
@@ -326,7 +329,7 @@ __device__ __forceinline__ void stage_weights(const MmaParams& p, const WGeom& W
 }
 
 template <int NT, int N>
-__global__ void __launch_bounds__(kW * 32, 2) k_mma24(const __grid_constant__ MmaParams pp) {
+__global__ void __launch_bounds__(kW * 32, kCtasPerSm) k_mma24(const __grid_constant__ MmaParams pp) {
   constexpr int CPC = N == 2 ? 64 : 128;   // dense columns per chunk
   constexpr int KT = CPC / 32;             // MMA k-steps per chunk
   extern __shared__ __align__(128) unsigned char smem[];
