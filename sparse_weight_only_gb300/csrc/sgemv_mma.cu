@@ -76,6 +76,10 @@ static_assert(kStages >= 2 && kStages <= 6, "sub-slice ring: 2..6 buffers");
 #define SGEMV_MMA_CUNROLL 2
 #endif
 constexpr int kChunkUnroll = SGEMV_MMA_CUNROLL;
+#ifndef SGEMV_MMA_GCHUNK
+#define SGEMV_MMA_GCHUNK 1
+#endif
+constexpr bool kGroupPerChunk = SGEMV_MMA_GCHUNK != 0;
 #ifndef SGEMV_MMA_NSUB_MIN
 #define SGEMV_MMA_NSUB_MIN 1
 #endif
@@ -497,7 +501,9 @@ __global__ void __launch_bounds__(kW * 32, kCtasPerSm) k_mma24(const __grid_cons
       for (int kt = 0; kt < KT; ++kt) {
         if (N == 1 && c * CPC + kt * 32 >= p.cols) break;   // ragged 1:4 tail
         int G = (c * CPC + kt * 32) >> p.gshift;
-        if (G != cur_group) {
+        // 2:4 chunks are 64 columns and groups at least as wide: only a
+        // chunk's first k-step can open a group
+        if ((N == 1 || kt == 0 || !kGroupPerChunk) && G != cur_group) {
           if (cur_group >= 0) {
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
