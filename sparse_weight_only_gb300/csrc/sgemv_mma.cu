@@ -80,6 +80,10 @@ constexpr int kChunkUnroll = SGEMV_MMA_CUNROLL;
 #define SGEMV_MMA_GCHUNK 1
 #endif
 constexpr bool kGroupPerChunk = SGEMV_MMA_GCHUNK != 0;
+#ifndef SGEMV_MMA_PULL4
+#define SGEMV_MMA_PULL4 1
+#endif
+constexpr bool kPullVec4 = SGEMV_MMA_PULL4 != 0;
 #ifndef SGEMV_MMA_NSUB_MIN
 #define SGEMV_MMA_NSUB_MIN 1
 #endif
@@ -206,6 +210,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 __device__ __forceinline__ uint32_t map_rank(uint32_t addr, int rank) {
   uint32_t r;
@@ -587,7 +599,41 @@ __global__ void __launch_bounds__(kW * 32, kCtasPerSm) k_mma24(const __grid_cons
       part[lr_g8 * mp + mc + 1] = acc[n][3];
     }
     cluster.sync();
-    {
+    if (kPullVec4) {
+      // four activation rows per load: 16-byte loads from every rank's
+      // partial tile (rows of mp floats, mp a multiple of 8), all ranks'
+      // loads in flight together, summed in rank order
+      const int nq = mp / 4;
+      const int n_el = (r_hi - r_lo) * nq;
+      const uint32_t part_s = (uint32_t)__cvta_generic_to_shared(part);
+      uint32_t rb[kMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kMaxSplit; ++q) rb[q] = map_rank(part_s, q < p.nsplit ? q : 0);
+      for (int e = threadIdx.x; e < n_el; e += kW * 32) {
+        const int lr = r_lo + e / nq, m4 = (e % nq) * 4;
+        const uint32_t off = (uint32_t)((lr * mp + m4) * 4);
+        float4 v[kMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+          v[q] = q < p.nsplit ? ld_cluster_f4(rb[q] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float sx = 0.0f, sy = 0.0f, sz = 0.0f, sw = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q) {
+          sx += v[q].x;
+          sy += v[q].y;
+          sz += v[q].z;
+          sw += v[q].w;
+        }
+        const int row = row0 + lr;
+        if (row < p.rows) {
+          __half* yr = p.y + row;
+          if (m4 < p.m) yr[(size_t)m4 * p.rows] = __float2half_rn(sx);
+          if (m4 + 1 < p.m) yr[(size_t)(m4 + 1) * p.rows] = __float2half_rn(sy);
+          if (m4 + 2 < p.m) yr[(size_t)(m4 + 2) * p.rows] = __float2half_rn(sz);
+          if (m4 + 3 < p.m) yr[(size_t)(m4 + 3) * p.rows] = __float2half_rn(sw);
+        }
+      }
+    } else {
       const int n_el = (r_hi - r_lo) * p.m;
       const float* rp[kMaxSplit];
 #pragma unroll
