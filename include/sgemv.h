@@ -156,7 +156,7 @@ int sgemv_export(sgemv_t h, uint8_t* vals, uint8_t* idx, uint16_t* scale,
  * CUDA-core decode kernel; batches (beam candidates, prefix-tree
  * verification nodes: the paper's parallel verification, section 3.1) run
  * on the sparse tensor cores with the 2-bit positions as the MMA's 2:4
- * metadata -- 2 <= m <= 24 with the warp-level sparse MMA, 25 <= m <= 64
+ * metadata -- 2 <= m <= 32 with the warp-level sparse MMA, 33 <= m <= 64
  * with tcgen05 and the accumulators in tensor memory.
  *   x_dev : m x cols binary16, row-major, 16-byte aligned, device memory;
  *   y_dev : m x rows binary16, row-major, 2-byte aligned, device memory,
@@ -190,14 +190,14 @@ int sgemv_run_host(sgemv_t h, const void* x_host, void* y_host, int m,
  * launch -- at most 8 of each N; the CTAs of one part take the 2:4 matrices
  * and those of the other the 1:4 ones, in proportion to their packed bytes,
  * and each CTA stages x and its lookup table once for all of its matrices
- * (more than 8 of one N: one launch per N and per 8).  With 2 <= m <= 24 the
+ * (more than 8 of one N: one launch per N and per 8).  With 2 <= m <= 32 the
  * matrices of one N share a launch of the batch kernel (at most 8 per
  * launch) when their row tiles still leave room to split K across a
  * cluster, else each runs alone; the outputs then match a single run within
  * the same tolerance, but the order of the fp32 partial sums may differ.
  * A device-side error of a shared launch (a bounded wait that ran out) is
  * recorded in the status word of the launch's first handle.  With
- * 25 <= m <= 64 the matrices of one N and group size share a launch of the
+ * 33 <= m <= 64 the matrices of one N and group size share a launch of the
  * tensor-core batch kernel (at most 4 per launch; the split-K partials use
  * the first handle's workspace).
  *   handles : count packed handles on one device, all with the same cols;
@@ -239,7 +239,7 @@ int sgemv_run_group_host(const sgemv_t* handles, int count, const void* x_host,
  * when max_m >= 2), a fixed array inside the library -- 10 MiB of fp32
  * partial tiles plus 64 KiB of per-tile counters -- that every GPU which
  * loads the library holds until the process exits.  It runs the tcgen05
- * batch kernel at every m (sgemv_run takes the warp-level one for m <= 24),
+ * batch kernel at every m (sgemv_run takes the warp-level one for m <= 32),
  * so for those m the order of the fp32 partial sums, not the tolerance, may
  * differ from sgemv_run's.  Limits: at most
  * 2,097,152 weight rows (16384 row tiles of 128) -> SGEMV_ERR_UNSUPPORTED
@@ -263,21 +263,22 @@ int sgemv_run_noalloc(sgemv_t h, const void* x_dev, void* y_dev, int m, void* st
  * issues all of its sends and no CTA retires before every CTA of its cluster
  * has issued them, so no late store lands in a retired CTA; what the limit
  * cannot guard against is a CTA that never reaches its sends (the launch
- * then does not finish).  9 <= m <= 24 reduce between cluster barriers that
- * every CTA reaches, with no such wait.  25 <= m <= 64: the waits for its
- * own TMA copies and MMAs -- it then stops issuing work, lets the copies it
- * issued land, frees its tensor memory and completes its split-K counters. */
+ * then does not finish).  9 <= m <= 32 reduce between cluster barriers that
+ * every CTA reaches, with no such wait.  33 <= m <= 64: the waits for
+ * its own TMA copies and MMAs -- it then stops issuing work, lets the copies
+ * it issued land, frees its tensor memory and completes its split-K
+ * counters. */
 int sgemv_status(sgemv_t h);
 
 /*
  * Failure-detection test hook (not a paper operation).  The next `runs`
- * batch products on this handle with 2 <= m <= 8 or 25 <= m <= 64 make
+ * batch products on this handle with 2 <= m <= 8 or 33 <= m <= 64 make
  * their bounded wait run out: for 2 <= m <= 8 every cluster rank withholds
- * its split-K partial sums, for m >= 25 the kernel withholds its x copies,
+ * its split-K partial sums, for m >= 33 the kernel withholds its x copies,
  * and the wait limit drops to about 20 microseconds.  sgemv_status then
  * returns SGEMV_ERR_TIMEOUT and y of those calls is undefined.  Nothing the
  * kernel waits for is in flight when it gives up, the device stays usable
- * and later calls run normally.  Calls with m = 1 or 9 <= m <= 24 (whose
+ * and later calls run normally.  Calls with m = 1 or 9 <= m <= 32 (whose
  * kernels wait on no copy, only on cluster barriers) do not consume the
  * hook.
  * runs = 0 cancels; runs < 0 -> SGEMV_ERR_ARG.

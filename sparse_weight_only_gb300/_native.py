@@ -257,7 +257,7 @@ class SparseGemv:
 
     def debug_withhold(self, runs: int) -> None:
         """Failure-detection test hook: the next `runs` batch products with
-        2 <= m <= 8 or m >= 25 make their bounded wait run out (sgemv_status
+        2 <= m <= 8 or m >= 33 make their bounded wait run out (sgemv_status
         then reports SGEMV_ERR_TIMEOUT)."""
         _check(load().sgemv_debug_withhold(self._h, runs), "sgemv_debug_withhold")
 

@@ -451,11 +451,11 @@ static int run_checked(sgemv_t h, const void* x, void* y, int m, cudaStream_t s)
     CUDA_TRY(cudaMemsetAsync(a.y, 0, (size_t)m * L.rows * sizeof(__half), s), "zero y");
     return SGEMV_OK;
   }
-  // m = 1: the CUDA-core pair-table kernel; 2 <= m <= kMmaSyncMaxM (24):
-  // the warp-level sparse MMA kernel; up to 64: the tcgen05 kernel (each
-  // measured the fastest in its range on the verification-batch layer set)
+  // m = 1: the CUDA-core pair-table kernel; 2 <= m <= mma_max_m(N) (32): the
+  // warp-level sparse MMA kernel; up to 64: the tcgen05 kernel (each
+  // measured the fastest in its range on the 7B layer shapes)
   cudaError_t e = m == 1                       ? sgemv::launch_m1(L, a, s)
-                  : m <= sgemv::kMmaSyncMaxM ? sgemv::launch_mma(L, a, s)
+                  : m <= sgemv::mma_max_m(L.n_keep) ? sgemv::launch_mma(L, a, s)
                                              : sgemv::launch_tc(L, a, h->tc, s);
   if (e == cudaErrorNotSupported) {
     (void)cudaGetLastError();
@@ -575,11 +575,11 @@ static int run_group_checked(const sgemv_t* handles, int count, const void* x_de
         if (int rc = run_checked(handles[i], x_dev, y_devs[i], m, s)) return rc;
       return SGEMV_OK;
     }
-    if (m > sgemv::kMmaSyncMaxM) {
-      // the tcgen05 kernel: one launch per (N, group size) and per
-      // tc_max_group() matrices
-      const int tcap = sgemv::tc_max_group();
-      for (int n = 1; n <= 2; ++n)
+    for (int n = 1; n <= 2; ++n) {
+      if (m > sgemv::mma_max_m(n)) {
+        // the tcgen05 kernel: one launch per group size and per
+        // tc_max_group() matrices of this N
+        const int tcap = sgemv::tc_max_group();
         for (int gs = 64; gs <= 256; gs *= 2) {
           sgemv::Layout Ls[8];
           sgemv::RunArgs as[8];
@@ -612,12 +612,10 @@ static int run_group_checked(const sgemv_t* handles, int count, const void* x_de
             }
           }
         }
-      return SGEMV_OK;
-    }
-    // 2 <= m <= kMmaSyncMaxM: one launch of the sparse MMA kernel per N and per
-    // max_group() matrices
-    const int cap = sgemv::max_group();
-    for (int n = 1; n <= 2; ++n) {
+        continue;
+      }
+      // the sparse MMA kernel: one launch per max_group() matrices of this N
+      const int cap = sgemv::max_group();
       sgemv::Layout Ls[8];
       sgemv::RunArgs as[8];
       int k = 0;

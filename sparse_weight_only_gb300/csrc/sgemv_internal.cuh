@@ -176,13 +176,18 @@ int report_cuda(cudaError_t e, const char* what);
 // Whether a product of m rows on this layout runs a kernel with the bounded
 // waits that the failure-detection hook can make run out.
 bool withhold_applies(const Layout& L, int m);
-// Largest m that the warp-level sparse MMA kernel (sgemv_mma.cu) takes;
-// larger batches run the tcgen05 kernel (sgemv_tc.cu).  Up to three n-tiles
-// the mma.sp kernel measured faster (layer steps at m = 17 / 24: 74-77 us
-// against 86 us); at four (m = 25..32) the tcgen05 kernel is.
-#ifndef SGEMV_MMA_MAX_M
-#define SGEMV_MMA_MAX_M 24
+// Largest m that the warp-level sparse MMA kernel (sgemv_mma.cu) takes, by
+// N; larger batches run the tcgen05 kernel (sgemv_tc.cu).  Measured on the
+// 7B layer shapes: the mma.sp kernel is faster up to four n-tiles (m <= 32).
+// 1:4 layers alone stay faster on it up to five (m <= 40), but a layer step
+// that then alternates the two kernels between launches lost that gain and
+// more, so both N switch at 32.
+#ifndef SGEMV_MMA_MAX_M2
+#define SGEMV_MMA_MAX_M2 32
 #endif
-constexpr int kMmaSyncMaxM = SGEMV_MMA_MAX_M;
+#ifndef SGEMV_MMA_MAX_M1
+#define SGEMV_MMA_MAX_M1 32
+#endif
+inline int mma_max_m(int n_keep) { return n_keep == 2 ? SGEMV_MMA_MAX_M2 : SGEMV_MMA_MAX_M1; }
 
 }  // namespace sgemv

@@ -1,5 +1,5 @@
 // sgemv_mma.cu -- SparseGemv for a small batch of activation rows on the
-// tensor cores with the warp-level sparse MMA: 2 <= m <= 24 (beam
+// tensor cores with the warp-level sparse MMA: 2 <= m <= 32 (beam
 // candidates / prefix-tree verification nodes; larger batches run the
 // tcgen05 kernel of sgemv_tc.cu, and this kernel takes any m <= 64), 2:4
 // weights and 1:4 weights (each kept weight paired with a zero).
@@ -817,11 +817,11 @@ int g_sms[64] = {0};
 }  // namespace
 
 bool withhold_applies(const Layout& L, int m) {
-  // one n-tile: this kernel's pushed split-K sums; m > kMmaSyncMaxM: the tcgen05
-  // kernel's x copies.  The pulled sums of wider tiles wait on cluster
-  // barriers only, which every rank reaches: nothing to withhold there.
+  // one n-tile: this kernel's pushed split-K sums; m > mma_max_m(N): the
+  // tcgen05 kernel's x copies.  The pulled sums of wider tiles wait on
+  // cluster barriers only, which every rank reaches: nothing to withhold.
   const bool pushed = push_reduce((m + 7) / 8);
-  return m >= 2 && (pushed || m > kMmaSyncMaxM) && L.rows > 0 && L.cols > 0;
+  return m >= 2 && (pushed || m > mma_max_m(L.n_keep)) && L.rows > 0 && L.cols > 0;
 }
 
 cudaError_t launch_mma_group(const Layout* Ls, const RunArgs* as, int count, cudaStream_t s) {

@@ -34,7 +34,7 @@ for rows, cols, n, g in shapes:
     h = swo.SparseGemv(rows, cols, n, g, max_m=64)
     h.pack(W)                                   # the packer too runs checked code
     norms = np.abs(oracle.dequant(p)).sum(axis=1)
-    for m in (1, 4, 16, 24, 33, 64):
+    for m in (1, 4, 16, 24, 32, 40, 48, 64):
         x = synth.activations(m + rows, m, cols)
         xd = torch.from_numpy(x).cuda()
         y = torch.empty((m, rows), dtype=torch.float16, device="cuda")

@@ -58,7 +58,7 @@ def test_config4_batch(native, orc, m):
         _check_gemv(native, orc, gv, m)
 
 
-@pytest.mark.parametrize("m", [4, 16, 24, 64])
+@pytest.mark.parametrize("m", [4, 16, 24, 40, 64])
 def test_layerset_batch_mixed(native, orc, m):
     """The config-3 layer set (2:4 and 1:4, groups 64..256) with M activation
     rows: the 1:4 matrices take the 2:4 sparse MMAs with zero partners."""

@@ -1,9 +1,9 @@
 """Failure detection on the GPU without a GPU fault.
 
 Every wait of the batch kernels on their own copies and MMAs is bounded
-(2 <= m <= 8: the pushed split-K sums; 25 <= m <= 64: the tcgen05 kernel's
-copies and MMAs; 9 <= m <= 24 waits on cluster barriers only).  The test
-hook sgemv_debug_withhold makes the kernel withhold its x
+(2 <= m <= 8: the pushed split-K sums; 33 <= m <= 64: the tcgen05 kernel's
+copies and MMAs; 9 <= m <= 32 waits on cluster barriers only).  The test hook
+sgemv_debug_withhold makes the kernel withhold its x
 loads (nothing is in flight that it would have to wait for) and shortens the
 limit: the wait runs out, the kernel records SGEMV_ERR_TIMEOUT in the
 handle's error word, lets the copies it did issue land, frees its tensor
@@ -36,7 +36,7 @@ def _run(h, x):
     return y
 
 
-@pytest.mark.parametrize("m", [2, 4, 8, 25, 33, 64])
+@pytest.mark.parametrize("m", [2, 4, 8, 33, 48, 64])
 def test_bounded_wait_runs_out_and_recovers(native, orc, m):
     rows, cols = 256, 4096          # two row tiles: clusters of several ranks
     h, p = _setup(native, orc, rows, cols, 2, 128, max_m=64)
@@ -75,9 +75,9 @@ def test_withhold_leaves_m1_alone(native, orc):
     h.debug_withhold(0)
 
 
-@pytest.mark.parametrize("m", [9, 16, 17, 24])
+@pytest.mark.parametrize("m", [9, 16, 17, 24, 25, 32])
 def test_withhold_leaves_pulled_sums_alone(native, orc, m):
-    """9 <= m <= 24 pulls the split-K sums between cluster barriers and
+    """9 <= m <= 32 pulls the split-K sums between cluster barriers and
     waits on no copy: the hook is not consumed and the result stays exact;
     the pending hook fires on the next call with a bounded wait."""
     rows, cols = 256, 4096

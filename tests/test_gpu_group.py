@@ -1,7 +1,7 @@
 """Grouped run (several matrices sharing x) through the C ABI.  Every output
 matches the oracle; at m = 1 it also equals the per-matrix run bit for bit
 (each row is computed the same way in either launch).  At m >= 2 the
-matrices of one N (and, from m = 25, one group size) share a launch of a
+matrices of one N (and, from m = 33, one group size) share a launch of a
 batch kernel, whose split of K across CTAs depends on the launch's tile
 count, so there the summation order -- not the tolerance -- may differ from
 a single run."""

@@ -138,7 +138,7 @@ def test_run_parity_small(native, orc, rows, cols, n_keep, group, dist, m):
             f"{rows}x{cols} N={n_keep} g={group} m={m}")
 
 
-@pytest.mark.parametrize("m", [1, 2, 4, 9, 16, 17, 24, 25, 32, 33, 64])
+@pytest.mark.parametrize("m", [1, 2, 4, 9, 16, 17, 24, 25, 32, 33, 40, 41, 48, 64])
 def test_run_parity_all_m(native, orc, m):
     rows, cols = 200, 1536
     for n_keep, group in ((2, 128), (1, 64)):
@@ -151,7 +151,7 @@ def test_run_parity_all_m(native, orc, m):
                 f"m={m} N={n_keep}")
 
 
-@pytest.mark.parametrize("n_keep,m", [(2, 25), (1, 33)])
+@pytest.mark.parametrize("n_keep,m", [(2, 33), (1, 41)])
 def test_run_parity_more_tiles_than_ctas(native, orc, n_keep, m):
     """The tcgen05 batch kernel's split-K with more 128-row tiles than CTAs: a CTA
     may cover a whole tile (written to y directly) before a shared one, so
